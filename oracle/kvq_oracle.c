@@ -36,7 +36,7 @@
  *    step recomputed from the stored zero, so every input lies in
  *    [z, z + (2^B-1) s] and the half-step bound survives storage; fp32 metadata
  *    is the literal formula;
- *  - a zero point of -0 is canonicalised to +0;
+ *  - a zero point or step of -0 is canonicalised to +0;
  *  - step == 0 (all values equal the stored zero) gives code 0;
  *  - symmetric range is +-(2^(B-1)-1) with scale = absmax / (2^(B-1)-1); the
  *    stored code is q + 2^(B-1);
@@ -147,10 +147,10 @@ void kvqo_quant_group(const float* x, long n, long stride, int bits, int sym, in
     float z, s;
     if (meta_f32) {
       z = mn + 0.0f;                      /* -0 -> +0 */
-      s = (mx - z) / (float)levels;
+      s = (mx - z) / (float)levels + 0.0f;
     } else {
       z = kvqo_f16_to_f32(kvqo_f32_to_f16(mn + 0.0f, KVQO_ROUND_DOWN));
-      float s32 = (mx - z) / (float)levels;
+      float s32 = (mx - z) / (float)levels + 0.0f; /* -0 -> +0 */
       s = kvqo_f16_to_f32(kvqo_f32_to_f16(s32, KVQO_ROUND_UP));
     }
     for (long i = 0; i < n; ++i) {

@@ -139,9 +139,9 @@ def test_zero_range_and_negative_zero():
     assert s == 0 and z == 1.5 and not codes.any()
     assert oracle.dequant_one(0, z, s, 4) == 1.5
     codes, z, s = oracle.quant_group(np.full(8, -0.0, np.float32), 3)
-    assert np.float32(z).view(np.uint32) == 0 and s == 0
+    assert np.float32(z).view(np.uint32) == 0 and np.float32(s).view(np.uint32) == 0
     codes, z, s = oracle.quant_group(np.full(8, -0.0, np.float32), 3, meta_f32=True)
-    assert np.float32(z).view(np.uint32) == 0
+    assert np.float32(z).view(np.uint32) == 0 and np.float32(s).view(np.uint32) == 0
 
 
 # ----------------------------------------------------------- tensor level ---
