@@ -1,0 +1,56 @@
+// kvq_internal.h — host-side cache handle and internal launcher declarations.
+#pragma once
+
+#include <string>
+#include <vector>
+
+#include "../../include/kvq.h"
+#include "kvq_common.cuh"
+
+struct kvq_cache {
+  kvq_config cfg;
+  int tcap = 0;          // token capacity of the tile / group layout
+  char* base = nullptr;  // caller's device buffer
+  size_t bytes = 0;
+  kvq::TensorLayout k, v;
+  int32_t* d_lens = nullptr;            // [layers][batch]
+  uint32_t* d_smax = nullptr;           // [2][layers][batch][kv_heads] largest step (float bits), K then V
+  uint32_t* d_append_tickets = nullptr; // [batch]
+  uint32_t* d_decode_tickets = nullptr; // [batch][kv_heads]
+  int* d_err = nullptr;                 // device error word
+  float* d_work = nullptr;              // split-K partials [batch][q_heads][max_chunks][head_dim + 2]
+  int max_chunks = 0;
+  std::vector<int32_t> lens;  // host mirror [layers][batch]
+  int last_launches = 0;
+  std::string last_error;
+  int device = 0;
+  int sm_count = 0;
+  int decode_path = 0;  // 0 = default (tensor-core kernel)
+};
+
+namespace kvq {
+
+struct LensArg {
+  int v[kMaxBatch];
+};
+
+inline long meta_groups(const kvq_cache* C, const TensorLayout& L) {
+  const long B = C->cfg.batch, H = C->cfg.kv_heads, D = C->cfg.head_dim;
+  if (L.axis == 1) return B * H * (C->tcap / L.group) * D;
+  if (L.whole) return B * C->tcap;
+  return B * H * C->tcap * L.gpt;
+}
+
+cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v, int x_f32,
+                           const int32_t* lens_host, long t_stride, cudaStream_t st, int* launches);
+cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, cudaStream_t st,
+                          int* launches);
+cudaError_t launch_export(kvq_cache* C, int layer, int is_value, uint8_t* codes, float* meta, uint16_t* tail,
+                          cudaStream_t st);
+size_t append_smem(const kvq_cache* C);
+
+// decode: plans the split, launches the split-K kernel (which also combines)
+cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
+                          cudaStream_t st, int* launches);
+
+}  // namespace kvq

@@ -1,0 +1,579 @@
+// kvq_quant.cu — quantize-and-pack kernels of libkvq: prefill, append with
+// group sealing, and the canonical export used for inspection.
+//
+// The quantizer follows "O Seu Cache KV Nao Tem um Problema de Bits. Tem um
+// Problema de Geometria", section "O Que o Erro de Quantizacao E Realmente
+// Feito" (zero = group minimum, step = range/(2^B-1), round to nearest) and the
+// symmetric form of "Kuantisasi KV Cache untuk Mengurangi Memory Inferensi Long
+// Context", section "Scale menentukan sistem koordinat kuantisasi".  Grouping
+// axes follow sections "Chaves..." (keys per channel along tokens) and
+// "Valores..." (values per token along channels); per-channel groups are only
+// sealed once G tokens exist, the newer tokens stay in an fp16 tail (section
+// "O Imposto dos Sistemas e Por Que Nao E um Detalhe").
+//
+// Group statistics are warp-shuffle min/max/absmax reductions; codes are
+// assembled into the fragment-ordered tile words of kvq_common.cuh and written
+// with 128-bit stores where a thread owns four consecutive words.
+#include "kvq_internal.h"
+
+namespace kvq {
+
+// ------------------------------------------------------- group statistics --
+
+// Warp-cooperative min / max / absmax over count values base[i*stride].
+__device__ __forceinline__ void warp_stats(const float* base, int count, int stride, float* mn, float* mx,
+                                           float* am) {
+  float a = INFINITY, b = -INFINITY, c = 0.0f;
+  for (int i = threadIdx.x & 31; i < count; i += 32) {
+    float v = base[(long)i * stride];
+    a = fminf(a, v);
+    b = fmaxf(b, v);
+    c = fmaxf(c, fabsf(v));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+    c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+  }
+  *mn = a;
+  *mx = b;
+  *am = c;
+}
+
+__device__ __forceinline__ float load_in(const void* p, long idx, int f32) {
+  return f32 ? reinterpret_cast<const float*>(p)[idx] : __half2float(reinterpret_cast<const __half*>(p)[idx]);
+}
+
+// Inverse of elem_pos: which (token, channel) of the tile a (lane, pair, half) holds.
+__device__ __forceinline__ void elem_of(int is_value, int lane, int pi, int e, int* t, int* c) {
+  int j = pi >> 2, r = pi & 3, rh = r & 1, kh = r >> 1;
+  int g = lane >> 2, tig = lane & 3;
+  int R = g + 8 * rh, kk = 2 * tig + 8 * kh + e;
+  if (is_value) {
+    *t = kk;
+    *c = 16 * j + R;
+  } else {
+    *t = R;
+    *c = 16 * j + kk;
+  }
+}
+
+// Value of tile word `wi` (0 .. D*bits/2-1) built from codes[t*D + c] (t < 16).
+__device__ __forceinline__ uint32_t build_word(const uint8_t* codes, int D, const Planes& pl, int is_value, int wi) {
+  // which plane
+  int p = 0;
+  for (int q = 1; q < pl.n; ++q)
+    if (wi >= D * pl.off[q] / 2) p = q;
+  int w = pl.w[p];
+  int W = D * w / 64, P = 16 / w;
+  int rel = wi - D * pl.off[p] / 2;
+  int lane = rel / W, i = rel % W;
+  uint32_t word = 0, mask = (1u << w) - 1u;
+  for (int k = 0; k < P; ++k) {
+    for (int e = 0; e < 2; ++e) {
+      int t, c;
+      elem_of(is_value, lane, i * P + k, e, &t, &c);
+      uint32_t code = codes[t * D + c];
+      word |= ((code >> pl.off[p]) & mask) << (k * w + 16 * e);
+    }
+  }
+  return word;
+}
+
+// Bits of tile word `wi` that belong to token row `trow`.
+__device__ __forceinline__ uint32_t word_token_mask(int D, const Planes& pl, int is_value, int wi, int trow) {
+  int p = 0;
+  for (int q = 1; q < pl.n; ++q)
+    if (wi >= D * pl.off[q] / 2) p = q;
+  int w = pl.w[p];
+  int W = D * w / 64, P = 16 / w;
+  int rel = wi - D * pl.off[p] / 2;
+  int lane = rel / W, i = rel % W;
+  uint32_t m = 0, mask = (1u << w) - 1u;
+  for (int k = 0; k < P; ++k)
+    for (int e = 0; e < 2; ++e) {
+      int t, c;
+      elem_of(is_value, lane, i * P + k, e, &t, &c);
+      if (t == trow) m |= mask << (k * w + 16 * e);
+    }
+  return m;
+}
+
+// Write the tile words of one 16-token tile (codes in shared memory, [16][D]).
+__device__ void store_tile(uint32_t* dst, const uint8_t* codes, int D, const TensorLayout& L, int is_value) {
+  int nw = L.tile_words;  // multiple of 32 (D*bits/2, D >= 64)
+  for (int q = threadIdx.x; q < nw / 4; q += blockDim.x) {
+    uint4 v;
+    v.x = build_word(codes, D, L.planes, is_value, 4 * q + 0);
+    v.y = build_word(codes, D, L.planes, is_value, 4 * q + 1);
+    v.z = build_word(codes, D, L.planes, is_value, 4 * q + 2);
+    v.w = build_word(codes, D, L.planes, is_value, 4 * q + 3);
+    reinterpret_cast<uint4*>(dst)[q] = v;
+  }
+}
+
+__device__ __forceinline__ void atomic_max_pos(uint32_t* addr, float v) {
+  // non-negative floats order like their bit patterns
+  if (v > 0.0f) atomicMax(addr, __float_as_uint(v));
+}
+
+// --------------------------------------------------------------- prefill ---
+
+struct QuantArgs {
+  TensorLayout L;
+  int is_value;
+  int layer, B, H, D, tcap, ntiles;
+  const void* x;  // [B][t_stride][H][D]
+  int x_f32;
+  long t_stride;
+  const int32_t* lens;  // device lens of this layer
+  char* base;           // cache buffer
+  uint32_t* smax;       // [B][H] for this tensor and layer
+};
+
+__device__ __forceinline__ uint32_t* codes_ptr(const QuantArgs& a, int b, int h, int tile) {
+  return reinterpret_cast<uint32_t*>(a.base + a.L.codes_off + a.layer * a.L.codes_layer) +
+         ((((long)b * a.H + h) * a.ntiles + tile) * a.L.tile_words);
+}
+__device__ __forceinline__ char* meta_ptr(const QuantArgs& a) {
+  return a.base + a.L.meta_off + a.layer * a.L.meta_layer;
+}
+__device__ __forceinline__ __half* tail_ptr(const QuantArgs& a, int b, int h) {
+  return reinterpret_cast<__half*>(a.base + a.L.tail_off + a.layer * a.L.tail_layer) +
+         (((long)b * a.H + h) * a.L.group) * a.D;
+}
+
+// Quantize a per-channel group block: G tokens x D channels of head h held in
+// shared memory as floats; writes the D metadata entries of group g and the
+// G/16 tiles.  All threads of the block participate.
+__device__ void quant_channel_block(const QuantArgs& a, int b, int h, int g, const float* xs, uint8_t* cs,
+                                    float* zs, float* ss) {
+  const int G = a.L.group, D = a.D;
+  const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  char* meta = meta_ptr(a);
+  float smax_local = 0.0f;
+  for (int c = warp; c < D; c += nwarp) {
+    float mn, mx, am;
+    warp_stats(xs + c, G, D, &mn, &mx, &am);
+    float z, s;
+    group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
+    if ((threadIdx.x & 31) == 0) {
+      zs[c] = z;
+      ss[c] = s;
+      long gi = (((long)b * a.H + h) * (a.tcap / G) + g) * D + c;
+      store_meta(meta, gi, a.L.meta_f32, a.L.sym, z, s);
+      smax_local = fmaxf(smax_local, s);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    int c = i % D;
+    cs[i] = (uint8_t)quant_code(xs[i], zs[c], ss[c], a.L.bits, a.L.sym);
+  }
+  __syncthreads();
+  for (int tt = 0; tt < G / kTile; ++tt)
+    store_tile(codes_ptr(a, b, h, (g * G) / kTile + tt), cs + tt * kTile * D, D, a.L, a.is_value);
+  if ((threadIdx.x & 31) == 0) atomic_max_pos(a.smax + (long)b * a.H + h, smax_local);
+}
+
+// Per-channel tensors: one CTA per (group, head, sequence).  The CTA of the
+// first unsealed group also writes the fp16 tail.
+__global__ void prefill_channel_kernel(QuantArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int G = a.L.group, D = a.D;
+  const int n = a.lens[b];
+  const int ng = n / G;
+  if (g > ng || (g == ng && n % G == 0)) return;
+  const long xs_t = (long)a.H * D;
+  const char* xb = reinterpret_cast<const char*>(a.x);
+  if (g == ng) {  // tail: tokens [ng*G, n) rounded to nearest fp16
+    __half* tail = tail_ptr(a, b, h);
+    int cnt = (n - ng * G) * D;
+    for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
+      int tt = i / D, c = i % D;
+      long src = ((long)b * a.t_stride + ng * G + tt) * xs_t + (long)h * D + c;
+      tail[(long)tt * D + c] = __float2half_rn(load_in(xb, src, a.x_f32));
+    }
+    return;
+  }
+  float* xs = reinterpret_cast<float*>(smem);
+  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + G * D);
+  float* zs = reinterpret_cast<float*>(cs + G * D);
+  float* ss = zs + D;
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    int tt = i / D, c = i % D;
+    long src = ((long)b * a.t_stride + (long)g * G + tt) * xs_t + (long)h * D + c;
+    // per-channel groups are formed from the fp16 staging precision of the tail
+    xs[i] = __half2float(__float2half_rn(load_in(xb, src, a.x_f32)));
+  }
+  __syncthreads();
+  quant_channel_block(a, b, h, g, xs, cs, zs, ss);
+}
+
+// Per-token tensors: one CTA per (tile, head, sequence); for whole-vector
+// groups one CTA per (tile, sequence) covering every head (blockIdx.y == 0).
+__global__ void prefill_token_kernel(QuantArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tile = blockIdx.x, b = blockIdx.z;
+  const int D = a.D;
+  const int n = a.lens[b];
+  if (tile * kTile >= n) return;
+  const int whole = a.L.whole;
+  const int h0 = whole ? 0 : blockIdx.y, nh = whole ? a.H : 1;
+  const int rowlen = nh * D;  // channels handled per token
+  const int G = whole ? rowlen : a.L.group;
+  const int gpr = rowlen / G;  // groups per token row in this CTA
+  float* xs = reinterpret_cast<float*>(smem);                       // [16][rowlen]
+  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kTile * rowlen);    // [nh][16][D]
+  float* zs = reinterpret_cast<float*>(cs + kTile * rowlen);        // [16*gpr]
+  float* ss = zs + kTile * gpr;
+  const long xs_t = (long)a.H * D;
+  for (int i = threadIdx.x; i < kTile * rowlen; i += blockDim.x) {
+    int tt = i / rowlen, c = i % rowlen;
+    int t = tile * kTile + tt;
+    xs[i] = t < n ? load_in(a.x, ((long)b * a.t_stride + t) * xs_t + (long)h0 * D + c, a.x_f32) : 0.0f;
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  char* meta = meta_ptr(a);
+  float smax_local = 0.0f;
+  for (int gi = warp; gi < kTile * gpr; gi += nwarp) {
+    int tt = gi / gpr, j = gi % gpr;
+    int t = tile * kTile + tt;
+    if (t >= n) continue;
+    float mn, mx, am;
+    warp_stats(xs + tt * rowlen + j * G, G, 1, &mn, &mx, &am);
+    float z, s;
+    group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
+    if ((threadIdx.x & 31) == 0) {
+      zs[gi] = z;
+      ss[gi] = s;
+      long mi = whole ? ((long)b * a.tcap + t) : ((((long)b * a.H + h0) * a.tcap + t) * gpr + j);
+      store_meta(meta, mi, a.L.meta_f32, a.L.sym, z, s);
+      smax_local = fmaxf(smax_local, s);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < kTile * rowlen; i += blockDim.x) {
+    int tt = i / rowlen, c = i % rowlen;
+    int t = tile * kTile + tt;
+    int hh = c / D, cc = c % D;
+    uint8_t code = 0;
+    if (t < n) code = (uint8_t)quant_code(xs[i], zs[tt * gpr + c / G], ss[tt * gpr + c / G], a.L.bits, a.L.sym);
+    cs[(hh * kTile + tt) * D + cc] = code;
+  }
+  __syncthreads();
+  for (int hh = 0; hh < nh; ++hh) store_tile(codes_ptr(a, b, h0 + hh, tile), cs + hh * kTile * D, D, a.L, a.is_value);
+  if ((threadIdx.x & 31) == 0 && smax_local > 0.0f)
+    for (int hh = 0; hh < nh; ++hh) atomic_max_pos(a.smax + (long)b * a.H + h0 + hh, smax_local);
+}
+
+__global__ void set_lens_kernel(int32_t* lens, LensArg la, int B) {
+  int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) lens[b] = la.v[b];
+}
+
+// ---------------------------------------------------------------- append ---
+
+struct AppendArgs {
+  QuantArgs k, v;       // x points at [B][H][D] new tokens (t_stride unused)
+  int32_t* lens;        // device lens of the layer
+  uint32_t* tickets;    // [B]
+};
+
+// Append the new token of (b, h) to one tensor.  `n` = old length.
+__device__ void append_tensor(const QuantArgs& a, int b, int h, int n, unsigned char* smem) {
+  const int D = a.D;
+  const long xs_t = (long)a.H * D;
+  const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
+  if (a.L.axis == 1) {  // per channel: tail, seal when full
+    const int G = a.L.group;
+    const int slot = n % G;
+    __half* tail = tail_ptr(a, b, h);
+    for (int c = threadIdx.x; c < D; c += blockDim.x)
+      tail[(long)slot * D + c] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
+    if (slot != G - 1) return;
+    __syncthreads();  // the block's own tail writes are visible to the block
+    float* xs = reinterpret_cast<float*>(smem);
+    uint8_t* cs = reinterpret_cast<uint8_t*>(xs + G * D);
+    float* zs = reinterpret_cast<float*>(cs + G * D);
+    float* ss = zs + D;
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) xs[i] = __half2float(tail[i]);
+    __syncthreads();
+    quant_channel_block(a, b, h, n / G, xs, cs, zs, ss);
+    __syncthreads();
+    return;
+  }
+  // per token: quantize the token row now and merge it into its tile
+  const int whole = a.L.whole;
+  const int nh = whole ? a.H : 1;
+  const int rowlen = nh * D;
+  const int G = whole ? rowlen : a.L.group;
+  const int gpr = rowlen / G;
+  float* xs = reinterpret_cast<float*>(smem);                  // [rowlen]
+  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + rowlen);       // [nh][16][D] (row trow only)
+  float* zs = reinterpret_cast<float*>(cs + kTile * rowlen);   // [gpr]
+  float* ss = zs + gpr;
+  for (int i = threadIdx.x; i < rowlen; i += blockDim.x) xs[i] = load_in(a.x, (long)b * xs_t + (long)h * D + i, a.x_f32);
+  __syncthreads();
+  char* meta = meta_ptr(a);
+  float smax_local = 0.0f;
+  for (int j = warp; j < gpr; j += nwarp) {
+    float mn, mx, am;
+    warp_stats(xs + j * G, G, 1, &mn, &mx, &am);
+    float z, s;
+    group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
+    if ((threadIdx.x & 31) == 0) {
+      zs[j] = z;
+      ss[j] = s;
+      long mi = whole ? ((long)b * a.tcap + n) : ((((long)b * a.H + h) * a.tcap + n) * gpr + j);
+      store_meta(meta, mi, a.L.meta_f32, a.L.sym, z, s);
+      smax_local = fmaxf(smax_local, s);
+    }
+  }
+  __syncthreads();
+  const int trow = n % kTile, tile = n / kTile;
+  for (int i = threadIdx.x; i < rowlen; i += blockDim.x) {
+    int hh = i / D, c = i % D;
+    cs[(hh * kTile + trow) * D + c] = (uint8_t)quant_code(xs[i], zs[i / G], ss[i / G], a.L.bits, a.L.sym);
+  }
+  __syncthreads();
+  for (int hh = 0; hh < nh; ++hh) {
+    uint32_t* dst = codes_ptr(a, b, h + hh, tile);
+    const uint8_t* tc = cs + hh * kTile * D;
+    for (int wi = threadIdx.x; wi < a.L.tile_words; wi += blockDim.x) {
+      uint32_t m = word_token_mask(D, a.L.planes, a.is_value, wi, trow);
+      if (!m) continue;
+      // build_word reads only row trow where m is set; other rows contribute garbage masked off below
+      uint32_t nv = 0;
+      {
+        int p = 0;
+        for (int q = 1; q < a.L.planes.n; ++q)
+          if (wi >= D * a.L.planes.off[q] / 2) p = q;
+        int w = a.L.planes.w[p];
+        int W = D * w / 64, P = 16 / w;
+        int rel = wi - D * a.L.planes.off[p] / 2;
+        int lane = rel / W, ii = rel % W;
+        uint32_t mk = (1u << w) - 1u;
+        for (int k = 0; k < P; ++k)
+          for (int e = 0; e < 2; ++e) {
+            int t, c;
+            elem_of(a.is_value, lane, ii * P + k, e, &t, &c);
+            if (t == trow) nv |= (((uint32_t)tc[t * D + c] >> a.L.planes.off[p]) & mk) << (k * w + 16 * e);
+          }
+      }
+      uint32_t old = (trow == 0) ? 0u : dst[wi];  // a fresh tile starts from zero bits
+      dst[wi] = (old & ~m) | nv;
+    }
+  }
+  if ((threadIdx.x & 31) == 0 && smax_local > 0.0f)
+    for (int hh = 0; hh < nh; ++hh) atomic_max_pos(a.smax + (long)b * a.H + h + hh, smax_local);
+  __syncthreads();
+}
+
+// One CTA per (sequence, kv head): append K then V; the last CTA of a
+// sequence advances its length (atomic ticket, no waiting).
+__global__ void append_kernel(AppendArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int b = blockIdx.x, h = blockIdx.y;
+  const int n = a.lens[b];
+  if (!(a.k.L.whole && h != 0)) append_tensor(a.k, b, h, n, smem);
+  __syncthreads();
+  if (!(a.v.L.whole && h != 0)) append_tensor(a.v, b, h, n, smem);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    unsigned prev = atomicAdd(a.tickets + b, 1u);
+    if (prev == (unsigned)gridDim.y - 1u) {
+      a.lens[b] = n + 1;
+      a.tickets[b] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+// ---------------------------------------------------------------- export ---
+
+struct ExportArgs {
+  QuantArgs a;
+  uint8_t* codes;    // [B][H][tcap][D] or null
+  float* meta;       // [groups][2] or null
+  uint16_t* tail;    // [B][H][G][D] or null
+};
+
+__device__ __forceinline__ int sealed_of(const TensorLayout& L, int n) {
+  return L.axis == 1 ? (n / L.group) * L.group : n;
+}
+
+// codes: one CTA per (tile, head, sequence)
+__global__ void export_codes_kernel(ExportArgs e) {
+  const QuantArgs& a = e.a;
+  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z, D = a.D;
+  const int ns = sealed_of(a.L, a.lens[b]);
+  const uint32_t* src = codes_ptr(a, b, h, tile);
+  for (int i = threadIdx.x; i < kTile * D; i += blockDim.x) {
+    int tt = i / D, c = i % D, t = tile * kTile + tt;
+    uint32_t code = 0;
+    if (t < ns) {
+      FragPos f = elem_pos(a.is_value, tt, c);
+      for (int p = 0; p < a.L.planes.n; ++p) {
+        int word, bit;
+        plane_word_bit(f, D, a.L.planes.w[p], a.L.planes.off[p], &word, &bit);
+        code |= ((src[word] >> bit) & ((1u << a.L.planes.w[p]) - 1u)) << a.L.planes.off[p];
+      }
+    }
+    e.codes[(((long)b * a.H + h) * a.tcap + t) * D + c] = (uint8_t)code;
+  }
+}
+
+// metadata: one thread per canonical group entry
+__global__ void export_meta_kernel(ExportArgs e, long ngroups) {
+  const QuantArgs& a = e.a;
+  long gi = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gi >= ngroups) return;
+  const int D = a.D;
+  int b, valid;
+  if (a.L.axis == 1) {
+    long per_b = (long)a.H * (a.tcap / a.L.group) * D;
+    b = (int)(gi / per_b);
+    long g = (gi / D) % (a.tcap / a.L.group);
+    valid = g < a.lens[b] / a.L.group;
+  } else if (a.L.whole) {
+    b = (int)(gi / a.tcap);
+    valid = (gi % a.tcap) < a.lens[b];
+  } else {
+    long per_b = (long)a.H * a.tcap * a.L.gpt;
+    b = (int)(gi / per_b);
+    long t = (gi / a.L.gpt) % a.tcap;
+    valid = t < a.lens[b];
+  }
+  float z = 0.0f, s = 0.0f;
+  if (valid) load_meta(meta_ptr(a), gi, a.L.meta_f32, a.L.sym, &z, &s);
+  e.meta[2 * gi] = z;
+  e.meta[2 * gi + 1] = s;
+}
+
+// tail: one CTA per (head, sequence)
+__global__ void export_tail_kernel(ExportArgs e) {
+  const QuantArgs& a = e.a;
+  const int h = blockIdx.y, b = blockIdx.z, D = a.D, G = a.L.group;
+  const int n = a.lens[b], cnt = n - (n / G) * G;
+  const __half* src = tail_ptr(a, b, h);
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
+    uint16_t v = (i / D) < cnt ? __half_as_ushort(src[i]) : (uint16_t)0;
+    e.tail[(((long)b * a.H + h) * G) * D + i] = v;
+  }
+}
+
+// ------------------------------------------------------------- launchers ---
+
+static QuantArgs make_args(const kvq_cache* C, int is_value, int layer, const void* x, int x_f32, long t_stride) {
+  QuantArgs a;
+  a.L = is_value ? C->v : C->k;
+  a.is_value = is_value;
+  a.layer = layer;
+  a.B = C->cfg.batch;
+  a.H = C->cfg.kv_heads;
+  a.D = C->cfg.head_dim;
+  a.tcap = C->tcap;
+  a.ntiles = C->tcap / kTile;
+  a.x = x;
+  a.x_f32 = x_f32;
+  a.t_stride = t_stride;
+  a.lens = C->d_lens + (long)layer * C->cfg.batch;
+  a.base = C->base;
+  a.smax = C->d_smax + ((long)is_value * C->cfg.layers + layer) * C->cfg.batch * C->cfg.kv_heads;
+  return a;
+}
+
+static size_t channel_smem(int G, int D) { return (size_t)G * D * 5 + (size_t)D * 8 + 16; }
+
+cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v, int x_f32,
+                           const int32_t* lens_host, long t_stride, cudaStream_t st, int* launches) {
+  const int B = C->cfg.batch, H = C->cfg.kv_heads, D = C->cfg.head_dim;
+  LensArg la;
+  for (int b = 0; b < B; ++b) la.v[b] = lens_host[b];
+  int32_t* dl = C->d_lens + (long)layer * B;
+  set_lens_kernel<<<(B + 127) / 128, 128, 0, st>>>(dl, la, B);
+  ++*launches;
+  // the layer's max-step statistics restart with the new contents
+  for (int is_v = 0; is_v < 2; ++is_v) {
+    uint32_t* sm = C->d_smax + ((long)is_v * C->cfg.layers + layer) * B * H;
+    cudaError_t e = cudaMemsetAsync(sm, 0, sizeof(uint32_t) * B * H, st);
+    if (e != cudaSuccess) return e;
+  }
+  int maxn = 0;
+  for (int b = 0; b < B; ++b) maxn = lens_host[b] > maxn ? lens_host[b] : maxn;
+  for (int is_v = 0; is_v < 2; ++is_v) {
+    QuantArgs a = make_args(C, is_v, layer, is_v ? v : k, x_f32, t_stride);
+    if (maxn == 0) continue;
+    if (a.L.axis == 1) {
+      size_t sm = channel_smem(a.L.group, D);
+      dim3 grid((maxn + a.L.group - 1) / a.L.group + 1, H, B);
+      cudaFuncSetAttribute(prefill_channel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      prefill_channel_kernel<<<grid, 256, sm, st>>>(a);
+    } else {
+      int nh = a.L.whole ? H : 1;
+      int rowlen = nh * D;
+      int gpr = a.L.whole ? 1 : D / a.L.group;
+      size_t sm = (size_t)kTile * rowlen * 5 + (size_t)kTile * gpr * 8 + 16;
+      dim3 grid((maxn + kTile - 1) / kTile, a.L.whole ? 1 : H, B);
+      cudaFuncSetAttribute(prefill_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      prefill_token_kernel<<<grid, 256, sm, st>>>(a);
+    }
+    ++*launches;
+  }
+  return cudaGetLastError();
+}
+
+size_t append_smem(const kvq_cache* C) {
+  const int H = C->cfg.kv_heads, D = C->cfg.head_dim;
+  size_t m = 0;
+  const TensorLayout* ls[2] = {&C->k, &C->v};
+  for (int i = 0; i < 2; ++i) {
+    const TensorLayout& L = *ls[i];
+    size_t s;
+    if (L.axis == 1) s = channel_smem(L.group, D);
+    else {
+      int rowlen = (L.whole ? H : 1) * D;
+      s = (size_t)rowlen * 4 + (size_t)kTile * rowlen + (size_t)rowlen * 8 + 16;
+    }
+    m = s > m ? s : m;
+  }
+  return m;
+}
+
+cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, cudaStream_t st,
+                          int* launches) {
+  AppendArgs a;
+  a.k = make_args(C, 0, layer, k, x_f32, 1);
+  a.v = make_args(C, 1, layer, v, x_f32, 1);
+  a.lens = C->d_lens + (long)layer * C->cfg.batch;
+  a.tickets = C->d_append_tickets;
+  size_t sm = append_smem(C);
+  cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  append_kernel<<<dim3(C->cfg.batch, C->cfg.kv_heads), 256, sm, st>>>(a);
+  ++*launches;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export(kvq_cache* C, int layer, int is_value, uint8_t* codes, float* meta, uint16_t* tail,
+                          cudaStream_t st) {
+  ExportArgs e;
+  e.a = make_args(C, is_value, layer, nullptr, 0, 0);
+  e.codes = codes;
+  e.meta = meta;
+  e.tail = tail;
+  const int B = C->cfg.batch, H = C->cfg.kv_heads;
+  if (codes) export_codes_kernel<<<dim3(C->tcap / kTile, H, B), 256, 0, st>>>(e);
+  if (meta) {
+    long ng = meta_groups(C, e.a.L);
+    export_meta_kernel<<<(unsigned)((ng + 255) / 256), 256, 0, st>>>(e, ng);
+  }
+  if (tail && e.a.L.axis == 1) export_tail_kernel<<<dim3(1, H, B), 256, 0, st>>>(e);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

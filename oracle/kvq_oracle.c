@@ -40,7 +40,9 @@
  *  - step == 0 (all values equal the stored zero) gives code 0;
  *  - symmetric range is +-(2^(B-1)-1) with scale = absmax / (2^(B-1)-1); the
  *    stored code is q + 2^(B-1);
- *  - the fp16 recent-token tail holds the input rounded to nearest fp16.
+ *  - the fp16 recent-token tail holds the input rounded to nearest fp16, and a
+ *    per-channel group is quantized from those fp16 values (so a prefill and a
+ *    token-by-token append of the same tokens build the same cache).
  */
 #include <math.h>
 #include <stdint.h>
@@ -237,13 +239,18 @@ int kvqo_quantize_tensor(const float* x, int batch, int tstride, int heads, int 
     const float* xb = x + b * xs_b;
     if (axis == KVQO_PER_CHANNEL) {
       long ng = n / group;
+      float* col = (float*)malloc(sizeof(float) * (size_t)group);
       for (int h = 0; h < heads; ++h) {
         for (long g = 0; g < ng; ++g) {
           for (int c = 0; c < dim; ++c) {
-            const float* src = xb + (g * group) * xs_t + (long)h * dim + c;
+            /* a per-channel group is formed from its tokens as held in the fp16
+               staging tail: the values are rounded to nearest fp16 first */
+            for (long t = 0; t < group; ++t)
+              col[t] = kvqo_f16_to_f32(
+                  kvqo_f32_to_f16(xb[(g * group + t) * xs_t + (long)h * dim + c], KVQO_ROUND_NEAREST));
             uint8_t* dst = codes + (((long)b * heads + h) * tcap + g * group) * dim + c;
             long mi = (((long)b * heads + h) * (tcap / group) + g) * dim + c;
-            kvqo_quant_group(src, group, xs_t, bits, sym, meta_f32, dst, dim, &meta[2 * mi], &meta[2 * mi + 1]);
+            kvqo_quant_group(col, group, 1, bits, sym, meta_f32, dst, dim, &meta[2 * mi], &meta[2 * mi + 1]);
           }
         }
         if (tail) {
@@ -256,6 +263,7 @@ int kvqo_quantize_tensor(const float* x, int batch, int tstride, int heads, int 
           }
         }
       }
+      free(col);
     } else if (group == heads * dim) {
       for (long t = 0; t < n; ++t) {
         /* the whole token vector (all heads) is one group; codes land per head */

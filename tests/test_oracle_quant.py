@@ -244,3 +244,22 @@ def test_outlier_channels_per_channel_keys_beat_per_token_keys():
         errs[axis] = e2[0].transpose(0, 2, 1)[ordinary].mean()
     # the ordinary channels pay for the outliers only under per-token grouping
     assert errs[oracle.PER_CHANNEL] < 0.1 * errs[oracle.PER_TOKEN]
+
+
+def test_per_channel_groups_use_the_fp16_staging_values():
+    """Tokens of an unsealed per-channel group wait in the fp16 tail, so a
+    sealed group is quantized from the fp16-rounded values; a prefix of a
+    sequence seals exactly the groups the longer sequence seals."""
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((1, 96, 2, 64)) * 3).astype(np.float32)  # fp32 source values
+    lens = np.array([96], np.int32)
+    a = oracle.quantize_tensor(x, lens, 96, 4, 32, oracle.PER_CHANNEL)
+    x16 = x.astype(np.float16).astype(np.float32)
+    b = oracle.quantize_tensor(x16, lens, 96, 4, 32, oracle.PER_CHANNEL)
+    np.testing.assert_array_equal(a["codes"], b["codes"])
+    np.testing.assert_array_equal(a["meta"], b["meta"])
+    pre = oracle.quantize_tensor(x, np.array([70], np.int32), 96, 4, 32, oracle.PER_CHANNEL)
+    np.testing.assert_array_equal(pre["codes"][:, :, :64], a["codes"][:, :, :64])
+    mp = pre["meta"].reshape(1, 2, 3, 64, 2)
+    ma = a["meta"].reshape(1, 2, 3, 64, 2)
+    np.testing.assert_array_equal(mp[:, :, :2], ma[:, :, :2])
