@@ -1,0 +1,385 @@
+"""Benchmark: quantized KV-cache decode step on GB300.
+
+One step = for every layer of the workload: kvq_append (one new token per
+sequence: quantize / stage / seal) then kvq_decode_attn (split-K attention over
+the packed cache).  The default workload is the GPT-2-small-shaped cache (12
+layers, batch 8, 12 heads, head_dim 64, 2048 cached tokens, fp16 N(0,1) with
+1% of key channels x10), K 4-bit per-channel G=32 / V 4-bit per-token G=32.
+
+The step is captured once as a CUDA graph of the public calls (planned for the
+full capacity, so one graph stays valid as the cache grows) and replayed.
+Between timed steps a 256 MB buffer is written to flush the 126 MB L2.
+
+  value : algorithmic decode bytes (packed codes + metadata + fp16 tail + q,
+          from kvq_decode_traffic) per step / device time of the step, inputs
+          already resident in HBM (the step's new tokens and queries are copied
+          device-to-device into the graph's input buffers inside the timed region)
+  e2e   : same metric with the inputs copied from pinned host memory and the
+          outputs copied back to pinned host memory inside the timed region
+  roofline : decode kernel alone; CUDA events recorded around every decode
+          launch inside the graph (on the launching stream)
+Under torchrun each rank runs its own shard of sequences (weak scaling, no
+data-path collective); rank 0 prints the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bit_quantized_kv_02_gb300 import build as kbuild  # noqa: E402
+from bit_quantized_kv_02_gb300 import dist as kdist  # noqa: E402
+from bit_quantized_kv_02_gb300 import kvq, synth  # noqa: E402
+
+METRIC = "decode-attn achieved HBM GB/s (% of peak) and cached tokens/s on 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+DECODE_SOURCES = ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_args.h", "kvq_common.cuh"]
+
+
+def workload(name: str, batch_scale=1) -> synth.Workload:
+    if name == "gpt2_small":
+        return synth.gpt2_small(kbits=4, vbits=4, kgroup=32, vgroup=32, kaxis=synth.PC, vaxis=synth.PT)
+    if name == "gpt2_small_k6v4":
+        return synth.gpt2_small(kbits=6, vbits=4, kgroup=64, vgroup=64, kaxis=synth.PT, vaxis=synth.PT)
+    if name == "llama2_13b":
+        return synth.llama2_13b()
+    if name == "wide_gqa":
+        return synth.wide_gqa()
+    if name == "serving_mix":
+        return synth.serving_mix()
+    if name == "tiny":
+        return synth.tiny()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def decode_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in DECODE_SOURCES:
+        h.update(open(os.path.join(ROOT, "bit_quantized_kv_02_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload_name: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", f"decode_kernel_{workload_name}.md")
+    if not os.path.exists(p):
+        return None
+    text = open(p).read()
+    m = re.search(r"decode_source_hash:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != decode_source_hash():
+        return None
+    return float(t.group(1))
+
+
+class Clocks:
+    """nvidia-smi sampler running during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, dev_index: int):
+        self.proc = None
+        self.dev = dev_index
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={dev_index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_event(external: bool):
+    if external:
+        try:
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+    return torch.cuda.Event(enable_timing=True)
+
+
+def run_ours(args, rank, world):
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    wl = workload(args.workload)
+    # weak scaling: each rank owns `batch` sequences of its own (its shard of the job)
+    B = wl.batch
+    L = wl.layers
+    steps, warm = args.steps, args.warmup
+    e2e_steps = min(steps, max(3, steps // 2))
+    cap = wl.max_tokens + warm + steps + e2e_steps + 2
+    cfg = kvq.make_config(L, B, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v)
+    cache = kvq.KVQCache(cfg, device=dev)
+    cache.kvq_set_decode_plan(cap)
+    # prefill every layer from GPU-generated synthetic data (layer by layer)
+    for l in range(L):
+        k, v = wl.layer_kv(l, dev, T=wl.max_tokens)
+        cache.kvq_prefill_quantize(l, k, v, wl.lens)
+        del k, v
+    torch.cuda.synchronize()
+    Hq, H, D = wl.q_heads, wl.kv_heads, wl.head_dim
+    nsteps = warm + steps
+    # per-step inputs, resident on the device; pinned host copies for e2e
+    kin_all = torch.stack([torch.stack(wl.step_kv(l, s, dev)) for s in range(nsteps) for l in range(L)])
+    kin_all = kin_all.view(nsteps, L, 2, B, H, D)
+    q_all = torch.stack([wl.layer_query(l, s, dev) for s in range(nsteps) for l in range(L)]).view(nsteps, L, B, Hq, D)
+    kin_host = kin_all.cpu().pin_memory()
+    q_host = q_all.cpu().pin_memory()
+    # static graph buffers
+    kin = torch.empty((L, 2, B, H, D), dtype=wl.dtype, device=dev)
+    qin = torch.empty((L, B, Hq, D), dtype=wl.dtype, device=dev)
+    out = torch.empty((L, B, Hq, D), dtype=torch.float32, device=dev)
+    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    scale = float(np.float32(1.0 / np.sqrt(D)))
+    ev_ext = [(make_event(True), make_event(True)) for _ in range(L)]
+    in_graph_timing = all(a is not None for a, _ in ev_ext)
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    kin.copy_(kin_all[0])
+    qin.copy_(q_all[0])
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        for l in range(L):
+            cache.kvq_append(l, kin[l, 0], kin[l, 1], stream=stream)
+            if in_graph_timing:
+                ev_ext[l][0].record(stream)
+            cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
+            if in_graph_timing:
+                ev_ext[l][1].record(stream)
+    launches_per_step = 2 * L
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def traffic():
+        cache.kvq_refresh_lens(stream)
+        return sum(cache.kvq_decode_traffic(l, kvq.F16) for l in range(L)), \
+            sum(sum(cache.kvq_get_lens(l)) for l in range(L))
+
+    def one_step(s, e2e: bool):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            if e2e:
+                kin.copy_(kin_host[s], non_blocking=True)
+                qin.copy_(q_host[s], non_blocking=True)
+            else:
+                kin.copy_(kin_all[s], non_blocking=True)
+                qin.copy_(q_all[s], non_blocking=True)
+            graph.replay()
+            if e2e:
+                out_host.copy_(out, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1)
+
+    # warm-up (untimed)
+    for s in range(warm):
+        one_step(s, False)
+    kdist.barrier()
+    clocks = Clocks(dev.index) if rank == 0 else None
+    t_steps, t_decode, tot_bytes, tot_tokens = 0.0, 0.0, 0.0, 0.0
+    for s in range(warm, nsteps):
+        t_steps += one_step(s, False)
+        if in_graph_timing:
+            t_decode += sum(a.elapsed_time(b) for a, b in ev_ext)
+        by, tk = traffic()
+        tot_bytes += by
+        tot_tokens += tk
+    clk = clocks.stop() if clocks else None
+    kdist.barrier()
+    # decode kernel alone when the graph could not hold timing events: eager launches, same stream
+    if not in_graph_timing:
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for l in range(L):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                ea.record(stream)
+                cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
+                eb.record(stream)
+            stream.synchronize()
+            t_decode += ea.elapsed_time(eb) * steps
+    # end-to-end: host inputs -> device -> host outputs, same graph
+    t_e2e = 0.0
+    for s in range(e2e_steps):
+        t_e2e += one_step(warm + s, True)
+    by_e2e = traffic()[0] * e2e_steps if e2e_steps else 0.0
+    # correctness guard: the device reported no timed-out wait
+    st = cache.kvq_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status {kvq.STATUS.get(st, st)}")
+
+    t_max = kdist.max_over_ranks(t_steps, device=dev)
+    bytes_all = kdist.sum_over_ranks(tot_bytes, device=dev)
+    tokens_all = kdist.sum_over_ranks(tot_tokens, device=dev)
+    t_e2e_max = kdist.max_over_ranks(t_e2e, device=dev)
+    bytes_e2e_all = kdist.sum_over_ranks(by_e2e, device=dev)
+    peak, peak_kind = measured_peaks()
+    res = None
+    if rank == 0:
+        value = bytes_all / (t_max * 1e-3) / 1e9
+        dec_bytes_per_launch = tot_bytes / (steps * L)
+        dec_ms_per_launch = t_decode / (steps * L)
+        achieved = dec_bytes_per_launch / (dec_ms_per_launch * 1e-3) / 1e9
+        h2d = kin.numel() * kin.element_size() + qin.numel() * qin.element_size()
+        d2h = out.numel() * out.element_size()
+        res = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(t_max / steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16 in, 2..8-bit codes, fp32 accumulate", "data": "synthetic",
+            "pct_of_peak": round(100.0 * value / peak, 2),
+            "cached_tokens_per_s": round(tokens_all / (t_max * 1e-3), 1),
+            "config": {"workload": wl.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": H,
+                       "head_dim": D, "cached_tokens": wl.lens[0], "k": list(wl.k), "v": list(wl.v),
+                       "k_format": "bits,group,axis(0 per-token,1 per-channel),mode(0 asym,1 sym)",
+                       "step": "per layer: kvq_append + kvq_decode_attn (CUDA graph)",
+                       "l2": "256 MB buffer written before every timed step (L2 flushed)",
+                       "parallelism": f"dp{world} (sequences sharded, no collective)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(wl.name),
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback",
+                         "kernel": "decode_kernel", "bytes_per_launch": round(dec_bytes_per_launch),
+                         "us_per_launch": round(dec_ms_per_launch * 1e3, 3),
+                         "timing": "events in graph around each decode launch" if in_graph_timing
+                         else "events around eager decode launches"},
+            "gpu_launches": launches_per_step * steps,
+            "e2e": {"value": round(bytes_e2e_all / (t_e2e_max * 1e-3) / 1e9, 2) if e2e_steps else None,
+                    "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "path": "pinned host -> device copies, graph of kvq_append + kvq_decode_attn, device -> host"},
+            "clocks": clk,
+        }
+    return res, wl
+
+
+def cpu_oracle_sample(wl, seconds=10.0, max_samples=64):
+    """Time the CPU oracle (dequantize + fp64 attention, single thread) on
+    (layer, sequence) samples of the workload until `seconds` have elapsed.
+    Returns (GB/s of the path's algorithmic decode bytes, description)."""
+    import oracle
+
+    D, H, Hq = wl.head_dim, wl.kv_heads, wl.q_heads
+    n = wl.lens[0]
+    k, v = wl.layer_kv(0, "cpu", T=n)
+    k, v = k[:1].contiguous(), v[:1].contiguous()
+    lens = np.array([n], np.int32)
+    q = wl.layer_query(0)[:1].float().numpy()
+    ok = oracle.quantize_tensor(k.float().numpy(), lens, n + (-n) % 128, *wl.k[:3], sym=bool(wl.k[3]))
+    ov = oracle.quantize_tensor(v.float().numpy(), lens, n + (-n) % 128, *wl.v[:3], sym=bool(wl.v[3]))
+    pk, mk, tk = oracle.tensor_bytes(1, H, D, lens, wl.k[0], wl.k[1], wl.k[2], bool(wl.k[3]))
+    pv, mv, tv = oracle.tensor_bytes(1, H, D, lens, wl.v[0], wl.v[1], wl.v[2], bool(wl.v[3]))
+    sample_bytes = pk + mk + tk + pv + mv + tv + Hq * D * 2
+    scale = np.float32(1.0 / np.sqrt(D))
+    t0 = time.perf_counter()
+    count = 0
+    while True:
+        kh = oracle.dequant_tensor(ok, lens, *wl.k[:3], sym=bool(wl.k[3]))
+        vh = oracle.dequant_tensor(ov, lens, *wl.v[:3], sym=bool(wl.v[3]))
+        oracle.attention(kh, vh, q, lens, scale)
+        count += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or count >= max_samples:
+            break
+    gbs = sample_bytes * count / el / 1e9
+    desc = (f"{count} x (one layer, one sequence: {n} tokens x {H} kv heads x {D}; dequantize + fp64 attention "
+            f"for {Hq} query heads), single thread, {el:.1f} s")
+    return gbs, desc, el / count
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gpt2_small")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, _ = kdist.rank_env()
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle; under torchrun only rank 0 works
+        if rank != 0:
+            return
+        wl = workload(args.workload)
+        import oracle
+        oracle.build()
+        gbs, desc, per = cpu_oracle_sample(wl, seconds=max(1.0, min(20.0, args.cpu_seconds * 0.5 *
+                                                                         (args.steps + args.warmup) / 25)))
+        cores = 1
+        line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp64 oracle",
+                "data": "synthetic", "config": {"workload": wl.name},
+                "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                 "sample": desc},
+                "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+    kbuild.build()
+    kvq.lib()
+    if world > 1:
+        kdist.init("nccl")
+    res, wl = run_ours(args, rank, world)
+    if rank == 0:
+        import oracle
+        oracle.build()
+        gbs, desc, _ = cpu_oracle_sample(wl, seconds=args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+        print(json.dumps(res))
+    if world > 1:
+        kdist.barrier()
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -222,6 +222,8 @@ kvq_status kvq_cache_create(const kvq_config* cfg, void* device_buf, size_t buf_
   C->lens.assign((size_t)cfg->layers * cfg->batch, 0);
   cudaError_t e = cudaGetDevice(&C->device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&C->sm_count, cudaDevAttrMultiProcessorCount, C->device);
+  if (e == cudaSuccess) e = quant_setup(C);
+  if (e == cudaSuccess) e = decode_setup(C);
   if (e == cudaSuccess) e = cudaMemsetAsync(device_buf, 0, need, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     delete C;
@@ -338,6 +340,21 @@ kvq_status kvq_device_status(kvq_cache_t C, void* stream) {
 }
 
 int kvq_last_launches(kvq_cache_t C) { return C ? C->last_launches : 0; }
+
+kvq_status kvq_set_decode_plan(kvq_cache_t C, int plan_tokens) {
+  if (!C || plan_tokens < 0) return KVQ_ERR_INVALID_ARG;
+  C->plan_tokens = plan_tokens;
+  return KVQ_OK;
+}
+
+kvq_status kvq_refresh_lens(kvq_cache_t C, void* stream) {
+  if (!C) return KVQ_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(C->lens.data(), C->d_lens, sizeof(int32_t) * C->lens.size(),
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return cuda_status(C, e);
+}
 
 const char* kvq_status_string(kvq_status s) {
   switch (s) {

@@ -1,6 +1,7 @@
 // kvq_decode.cu — split planning and launch of the decode attention kernel.
 #include <algorithm>
 #include <cmath>
+#include <vector>
 
 #include "kvq_decode_args.h"
 
@@ -67,22 +68,25 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   if (a.warp_bytes * kWarps < merge_bytes) a.warp_bytes = round_up((merge_bytes + kWarps - 1) / kWarps, 128);
   a.head_bytes = round_up((rep * D + (C->k.axis == 0 ? C->k.gpt * rep : 0)) * 4, 128);
   P->smem = (size_t)a.head_bytes + (size_t)kWarps * a.warp_bytes;
-  void* fn = pick_kernel(D, r8, C->v.axis);
-  if (!fn) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P->smem);
-  if (e != cudaSuccess) return e;
-  int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kWarps * 32, P->smem);
-  if (e != cudaSuccess) return e;
-  *occ_out = std::max(occ, 1);
+  if (!pick_kernel(D, r8, C->v.axis)) return cudaErrorInvalidValue;
+  *occ_out = C->dec_occ;
   return cudaSuccess;
 }
 
-size_t decode_smem_bytes(kvq_cache* C) {
+cudaError_t decode_setup(kvq_cache* C) {
   Plan P;
-  int occ;
-  if (make_plan(C, 0, &P, &occ) != cudaSuccess) return 0;
-  return P.smem;
+  int occ = 1;
+  cudaError_t e = make_plan(C, 0, &P, &occ);
+  if (e != cudaSuccess) return e;
+  void* fn = pick_kernel(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
+  if (P.smem > 227 * 1024) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.smem);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kWarps * 32, P.smem);
+  if (e != cudaSuccess) return e;
+  C->dec_smem = P.smem;
+  C->dec_occ = std::max(occ, 1);
+  return cudaSuccess;
 }
 
 // Choose tokens per CTA (a multiple of 4 warps x the alignment unit) so that
@@ -129,7 +133,11 @@ cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, flo
   int unit = kTile;
   if (C->k.axis == 1) unit = std::max(unit, C->k.group);
   if (C->v.axis == 1) unit = std::max(unit, C->v.group);
-  const int32_t* lens = C->lens.data() + (long)layer * cfg.batch;
+  // plan on the host length mirror, raised to the plan hint (a launch planned
+  // for the hint stays valid while the cache grows up to it)
+  std::vector<int32_t> plan(C->lens.begin() + (long)layer * cfg.batch, C->lens.begin() + (long)(layer + 1) * cfg.batch);
+  for (auto& x : plan) x = std::max(x, (int32_t)std::min(C->plan_tokens, C->cfg.max_tokens));
+  const int32_t* lens = plan.data();
   const int slots = C->sm_count * occ;
   a.S = choose_split(C, lens, unit, slots, C->max_chunks);
   a.Sw = a.S / kWarps;
@@ -143,7 +151,7 @@ cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, flo
   void* fn = pick_kernel(cfg.head_dim, cfg.q_heads / cfg.kv_heads == 8, C->v.axis);
   dim3 grid(nch, cfg.kv_heads, cfg.batch);
   void* args[] = {&a};
-  e = cudaLaunchKernel(fn, grid, dim3(kWarps * 32), args, P.smem, st);
+  e = cudaLaunchKernel(fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
   ++*launches;
   return e;
 }

@@ -25,7 +25,9 @@ struct kvq_cache {
   std::string last_error;
   int device = 0;
   int sm_count = 0;
-  int decode_path = 0;  // 0 = default (tensor-core kernel)
+  int plan_tokens = 0;  // decode split plan assumes at least this many tokens per sequence
+  size_t dec_smem = 0;  // dynamic shared memory of the decode kernel
+  int dec_occ = 1;      // resident decode CTAs per SM
 };
 
 namespace kvq {
@@ -48,6 +50,10 @@ cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v,
 cudaError_t launch_export(kvq_cache* C, int layer, int is_value, uint8_t* codes, float* meta, uint16_t* tail,
                           cudaStream_t st);
 size_t append_smem(const kvq_cache* C);
+
+// one-time kernel attribute set-up at cache creation (keeps launches capturable)
+cudaError_t quant_setup(kvq_cache* C);
+cudaError_t decode_setup(kvq_cache* C);
 
 // decode: plans the split, launches the split-K kernel (which also combines)
 cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,

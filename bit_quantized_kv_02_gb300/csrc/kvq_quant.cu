@@ -14,6 +14,8 @@
 // Group statistics are warp-shuffle min/max/absmax reductions; codes are
 // assembled into the fragment-ordered tile words of kvq_common.cuh and written
 // with 128-bit stores where a thread owns four consecutive words.
+#include <algorithm>
+
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -489,6 +491,7 @@ static QuantArgs make_args(const kvq_cache* C, int is_value, int layer, const vo
 }
 
 static size_t channel_smem(int G, int D) { return (size_t)G * D * 5 + (size_t)D * 8 + 16; }
+static size_t token_smem(const kvq_cache* C, const TensorLayout& L);
 
 cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v, int x_f32,
                            const int32_t* lens_host, long t_stride, cudaStream_t st, int* launches) {
@@ -512,15 +515,10 @@ cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v
     if (a.L.axis == 1) {
       size_t sm = channel_smem(a.L.group, D);
       dim3 grid((maxn + a.L.group - 1) / a.L.group + 1, H, B);
-      cudaFuncSetAttribute(prefill_channel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       prefill_channel_kernel<<<grid, 256, sm, st>>>(a);
     } else {
-      int nh = a.L.whole ? H : 1;
-      int rowlen = nh * D;
-      int gpr = a.L.whole ? 1 : D / a.L.group;
-      size_t sm = (size_t)kTile * rowlen * 5 + (size_t)kTile * gpr * 8 + 16;
+      size_t sm = token_smem(C, a.L);
       dim3 grid((maxn + kTile - 1) / kTile, a.L.whole ? 1 : H, B);
-      cudaFuncSetAttribute(prefill_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       prefill_token_kernel<<<grid, 256, sm, st>>>(a);
     }
     ++*launches;
@@ -553,10 +551,31 @@ cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v,
   a.lens = C->d_lens + (long)layer * C->cfg.batch;
   a.tickets = C->d_append_tickets;
   size_t sm = append_smem(C);
-  cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   append_kernel<<<dim3(C->cfg.batch, C->cfg.kv_heads), 256, sm, st>>>(a);
   ++*launches;
   return cudaGetLastError();
+}
+
+static size_t token_smem(const kvq_cache* C, const TensorLayout& L) {
+  const int rowlen = (L.whole ? C->cfg.kv_heads : 1) * C->cfg.head_dim;
+  const int gpr = L.whole ? 1 : C->cfg.head_dim / L.group;
+  return (size_t)kTile * rowlen * 5 + (size_t)kTile * gpr * 8 + 16;
+}
+
+cudaError_t quant_setup(kvq_cache* C) {
+  size_t chan = 0, tok = 0;
+  const TensorLayout* ls[2] = {&C->k, &C->v};
+  for (int i = 0; i < 2; ++i) {
+    if (ls[i]->axis == 1) chan = std::max(chan, channel_smem(ls[i]->group, C->cfg.head_dim));
+    else tok = std::max(tok, token_smem(C, *ls[i]));
+  }
+  cudaError_t e = cudaSuccess;
+  if (chan) e = cudaFuncSetAttribute(prefill_channel_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chan);
+  if (e == cudaSuccess && tok)
+    e = cudaFuncSetAttribute(prefill_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tok);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)append_smem(C));
+  return e;
 }
 
 cudaError_t launch_export(kvq_cache* C, int layer, int is_value, uint8_t* codes, float* meta, uint16_t* tail,

@@ -55,7 +55,8 @@ _lib = None
 
 EXPORTED = ["kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_prefill_quantize", "kvq_append",
             "kvq_decode_attn", "kvq_export", "kvq_cache_tcap", "kvq_get_lens", "kvq_decode_traffic",
-            "kvq_device_status", "kvq_last_launches", "kvq_status_string", "kvq_last_error"]
+            "kvq_device_status", "kvq_last_launches", "kvq_status_string", "kvq_last_error",
+            "kvq_set_decode_plan", "kvq_refresh_lens"]
 
 
 def lib():
@@ -84,11 +85,13 @@ def lib():
         L.kvq_last_launches.restype = I
         L.kvq_status_string.argtypes = [S]
         L.kvq_status_string.restype = ctypes.c_char_p
+        L.kvq_set_decode_plan.argtypes = [P, I]
+        L.kvq_refresh_lens.argtypes = [P, P]
         L.kvq_last_error.argtypes = [P]
         L.kvq_last_error.restype = ctypes.c_char_p
         for name in ("kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_prefill_quantize",
                      "kvq_append", "kvq_decode_attn", "kvq_export", "kvq_get_lens", "kvq_decode_traffic",
-                     "kvq_device_status"):
+                     "kvq_device_status", "kvq_set_decode_plan", "kvq_refresh_lens"):
             getattr(L, name).restype = S
         _lib = L
         return L
@@ -231,6 +234,12 @@ class KVQCache:
 
     def kvq_device_status(self, stream=None) -> int:
         return lib().kvq_device_status(self.handle, _stream(stream))
+
+    def kvq_set_decode_plan(self, plan_tokens: int):
+        _check(lib().kvq_set_decode_plan(self.handle, int(plan_tokens)), "kvq_set_decode_plan")
+
+    def kvq_refresh_lens(self, stream=None):
+        _check(lib().kvq_refresh_lens(self.handle, _stream(stream)), "kvq_refresh_lens", self.handle)
 
     def kvq_last_launches(self) -> int:
         return lib().kvq_last_launches(self.handle)

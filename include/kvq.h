@@ -181,6 +181,18 @@ kvq_status kvq_decode_traffic(kvq_cache_t cache, int layer, int q_dtype, double*
  * then cleared) or a CUDA error is pending (KVQ_ERR_CUDA). */
 kvq_status kvq_device_status(kvq_cache_t cache, void* stream);
 
+/* Decode split plan hint: when plan_tokens > 0, kvq_decode_attn sizes its
+ * split-K launch as if every sequence held max(its length, plan_tokens) tokens
+ * (CTAs past a sequence's real length exit at once).  A launch planned this way
+ * stays valid while the cache grows up to plan_tokens, which is what a CUDA
+ * graph that captured kvq_append + kvq_decode_attn and is replayed step after
+ * step needs.  0 (default) plans for the current lengths. */
+kvq_status kvq_set_decode_plan(kvq_cache_t cache, int plan_tokens);
+
+/* Replayed graphs advance the device lengths only; this copies them back into
+ * the host mirror (synchronises `stream`). */
+kvq_status kvq_refresh_lens(kvq_cache_t cache, void* stream);
+
 /* Number of kernel launches the last kvq_decode_attn / kvq_append /
  * kvq_prefill_quantize call on this handle issued. */
 int kvq_last_launches(kvq_cache_t cache);
