@@ -156,4 +156,40 @@ cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, flo
   return e;
 }
 
+// Same plan and kernel as launch_decode, with the split-K partials and the
+// combine tickets placed in caller-chosen scratch (used by the entry point
+// whose scratch is a static device array).
+cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
+                                  cudaStream_t st, int* launches, float* work, uint32_t* tickets) {
+  Plan P;
+  int occ = 1;
+  cudaError_t e = make_plan(C, layer, &P, &occ);
+  if (e != cudaSuccess) return e;
+  DecodeArgs& a = P.a;
+  a.work = work;
+  a.tickets = tickets;
+  const kvq_config& cfg = C->cfg;
+  int unit = kTile;
+  if (C->k.axis == 1) unit = std::max(unit, C->k.group);
+  if (C->v.axis == 1) unit = std::max(unit, C->v.group);
+  std::vector<int32_t> plan(C->lens.begin() + (long)layer * cfg.batch, C->lens.begin() + (long)(layer + 1) * cfg.batch);
+  for (auto& x : plan) x = std::max(x, (int32_t)std::min(C->plan_tokens, C->cfg.max_tokens));
+  const int slots = C->sm_count * occ;
+  a.S = choose_split(C, plan.data(), unit, slots, C->max_chunks);
+  a.Sw = a.S / kWarps;
+  int maxn = 0;
+  for (int b = 0; b < cfg.batch; ++b) maxn = std::max(maxn, (int)plan[b]);
+  const int nch = std::max(1, (maxn + a.S - 1) / a.S);
+  a.q = q;
+  a.q_f32 = q_f32;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out;
+  void* fn = pick_kernel(cfg.head_dim, cfg.q_heads / cfg.kv_heads == 8, C->v.axis);
+  dim3 grid(nch, cfg.kv_heads, cfg.batch);
+  void* args[] = {&a};
+  e = cudaLaunchKernel(fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
+  ++*launches;
+  return e;
+}
+
 }  // namespace kvq

@@ -59,4 +59,7 @@ cudaError_t decode_setup(kvq_cache* C);
 cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
                           cudaStream_t st, int* launches);
 
+cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
+                                  cudaStream_t st, int* launches, float* work, uint32_t* tickets);
+
 }  // namespace kvq

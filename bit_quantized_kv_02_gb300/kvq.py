@@ -56,7 +56,7 @@ _lib = None
 EXPORTED = ["kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_prefill_quantize", "kvq_append",
             "kvq_decode_attn", "kvq_export", "kvq_cache_tcap", "kvq_get_lens", "kvq_decode_traffic",
             "kvq_device_status", "kvq_last_launches", "kvq_status_string", "kvq_last_error",
-            "kvq_set_decode_plan", "kvq_refresh_lens"]
+            "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static"]
 
 
 def lib():
@@ -85,13 +85,14 @@ def lib():
         L.kvq_last_launches.restype = I
         L.kvq_status_string.argtypes = [S]
         L.kvq_status_string.restype = ctypes.c_char_p
+        L.kvq_decode_attn_static.argtypes = [P, I, P, I, ctypes.c_float, P, P]
         L.kvq_set_decode_plan.argtypes = [P, I]
         L.kvq_refresh_lens.argtypes = [P, P]
         L.kvq_last_error.argtypes = [P]
         L.kvq_last_error.restype = ctypes.c_char_p
         for name in ("kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_prefill_quantize",
                      "kvq_append", "kvq_decode_attn", "kvq_export", "kvq_get_lens", "kvq_decode_traffic",
-                     "kvq_device_status", "kvq_set_decode_plan", "kvq_refresh_lens"):
+                     "kvq_device_status", "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static"):
             getattr(L, name).restype = S
         _lib = L
         return L
@@ -192,6 +193,17 @@ class KVQCache:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         _check(lib().kvq_decode_attn(self.handle, layer, _ptr(q), _dtype_code(q), float(scale), _ptr(out),
                                      _stream(stream)), "kvq_decode_attn", self.handle)
+        return out
+
+    def kvq_decode_attn_static(self, layer: int, q: torch.Tensor, out: torch.Tensor | None = None,
+                               scale: float = 0.0, stream=None) -> torch.Tensor:
+        """kvq_decode_attn with its scratch in the library's static device array
+        (for callers that cannot provide device memory); same inputs and output."""
+        assert q.is_contiguous()
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        _check(lib().kvq_decode_attn_static(self.handle, layer, _ptr(q), _dtype_code(q), float(scale), _ptr(out),
+                                            _stream(stream)), "kvq_decode_attn_static", self.handle)
         return out
 
     def kvq_export(self, layer: int, stream=None) -> dict:

@@ -152,6 +152,26 @@ kvq_status kvq_append(kvq_cache_t cache, int layer, const void* k_new, const voi
 kvq_status kvq_decode_attn(kvq_cache_t cache, int layer, const void* q, int q_dtype, float softmax_scale,
                            float* out, void* stream);
 
+/* kvq_decode_attn without scratch memory from the caller: identical inputs,
+ * output and numerics, but the split-K partials and combine tickets live in a
+ * 16 MiB array compiled into libkvq (static device memory, held by every GPU
+ * that loads the library until the process exits).  For callers that cannot
+ * allocate or reserve device memory beyond what they already planned: e.g. a
+ * runtime whose device memory is laid out once by another component, or a
+ * plugin that must not call cudaMalloc.  Allocates nothing.  The source pages
+ * have no counterpart of this call; it is a deployment convenience.
+ *  - Needs batch * q_heads * max_chunks * (head_dim + 2) * 4 bytes (rounded up
+ *    to 256) + batch * kv_heads * 4 bytes <= 16 MiB, else KVQ_ERR_BUFFER_TOO_SMALL
+ *    (nothing launched; kvq_last_error says how much was needed).
+ *  - The first call on a device looks up the array's device address with that
+ *    device current (cudaGetSymbolAddress); make that first call before any
+ *    stream capture.
+ *  - Every call shares the one array and finds the last call's contents in it:
+ *    the tickets are cleared at each call, and calls that overlap on the GPU
+ *    (different streams, handles or threads) race with each other. */
+kvq_status kvq_decode_attn_static(kvq_cache_t cache, int layer, const void* q, int q_dtype, float softmax_scale,
+                                  float* out, void* stream);
+
 /* Canonical copy of layer `layer` for inspection and tests (device pointers,
  * any may be NULL to skip):
  *   codes_k/v : uint8  [batch][kv_heads][tcap][head_dim], one code per element
