@@ -347,6 +347,16 @@ kvq_status kvq_set_decode_plan(kvq_cache_t C, int plan_tokens) {
   return KVQ_OK;
 }
 
+kvq_status kvq_set_decode_kernel(kvq_cache_t C, int which) {
+  if (!C || (which != 0 && which != 1)) return KVQ_ERR_INVALID_ARG;
+  C->generic_decode = which;
+  return cuda_status(C, decode_setup(C));
+}
+
+int kvq_decode_kernel_specialized(kvq_cache_t C) {
+  return (C && C->dec_fn && C->dec_fn == decode_kernel_fast(C) && !C->generic_decode) ? 1 : 0;
+}
+
 kvq_status kvq_refresh_lens(kvq_cache_t C, void* stream) {
   if (!C) return KVQ_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

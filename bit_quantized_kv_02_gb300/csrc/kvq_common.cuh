@@ -221,9 +221,9 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Bounded wait on an mbarrier phase: gives up after ~1 s, records the failure
-// in *err and returns false.  Never spins forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+// in *err and returns false.  Never spins forever.  The slow path is out of
+// line so the common case (data already landed) costs one test.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int* err) {
   uint64_t t0 = global_timer_ns();
   for (int it = 0; it < (1 << 30); ++it) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -231,6 +231,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
   if (err) atomicExch(err, 1);
   return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, err);
 }
 
 __device__ __forceinline__ void mma_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,

@@ -35,50 +35,67 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   const int D = cfg.head_dim, rep = cfg.q_heads / cfg.kv_heads;
   const bool r8 = rep == 8;
   DecodeArgs& a = P->a;
-  a.K = C->k;
-  a.V = C->v;
-  a.layer = layer;
+  auto fill = [&](DecTensor& d, const TensorLayout& L) {
+    d.codes = C->base + L.codes_off + (size_t)layer * L.codes_layer;
+    d.meta = C->base + L.meta_off + (size_t)layer * L.meta_layer;
+    d.tail = reinterpret_cast<const __half*>(C->base + L.tail_off + (size_t)layer * L.tail_layer);
+    d.bits = L.bits;
+    d.sym = L.sym;
+    d.meta_f32 = L.meta_f32;
+    d.axis = L.axis;
+    d.whole = L.whole;
+    d.group = L.whole ? D : L.group;
+    int lg = 0;
+    while ((1 << lg) < d.group) ++lg;
+    d.lg_group = L.whole ? 30 : lg;
+    d.gpt = L.gpt;
+    d.meta_bytes = L.meta_bytes;
+    d.tile_bytes = L.tile_words * 4;
+    d.mtile_bytes = L.axis == 0 ? meta_tile_bytes(L) : D * L.meta_bytes;
+  };
+  fill(a.K, C->k);
+  fill(a.V, C->v);
   a.B = cfg.batch;
   a.H = cfg.kv_heads;
   a.rep = rep;
   a.tcap = C->tcap;
   a.ntiles = C->tcap / kTile;
-  a.base = C->base;
   a.lens = C->d_lens + (long)layer * cfg.batch;
+  a.smax_k = C->d_smax + ((long)0 * cfg.layers + layer) * cfg.batch * cfg.kv_heads;
   a.smax_v = C->d_smax + ((long)1 * cfg.layers + layer) * cfg.batch * cfg.kv_heads;
   a.max_chunks = C->max_chunks;
   a.work = C->d_work;
   a.tickets = C->d_decode_tickets;
   a.err = C->d_err;
-  a.kc_bytes = C->k.tile_words * 4;
-  a.vc_bytes = C->v.tile_words * 4;
-  a.km_tile_bytes = C->k.axis == 0 ? meta_tile_bytes(C->k) : 0;
-  a.vm_tile_bytes = C->v.axis == 0 ? meta_tile_bytes(C->v) : 0;
-  a.km_group_bytes = C->k.axis == 1 ? D * C->k.meta_bytes : 0;
-  a.vm_group_bytes = C->v.axis == 1 ? D * C->v.meta_bytes : 0;
-  a.st_kc = 0;
-  a.st_km = round_up(a.st_kc + a.kc_bytes, 16);
-  a.st_vc = round_up(a.st_km + std::max(a.km_tile_bytes, a.km_group_bytes), 16);
-  a.st_vm = round_up(a.st_vc + a.vc_bytes, 16);
-  a.stage_bytes = round_up(a.st_vm + std::max(a.vm_tile_bytes, a.vm_group_bytes), 128);
-  a.nstages = a.stage_bytes <= 4096 ? 4 : 3;
-  a.barea_bytes = (D / 16) * 32 * 8 * (r8 ? 2 : 1);
-  a.warp_bytes = round_up(a.barea_bytes + 128 + a.nstages * a.stage_bytes + a.nstages * 8, 128);
-  const int merge_bytes = kWarps * rep * (D + 2) * 4;
-  if (a.warp_bytes * kWarps < merge_bytes) a.warp_bytes = round_up((merge_bytes + kWarps - 1) / kWarps, 128);
-  a.head_bytes = round_up((rep * D + (C->k.axis == 0 ? C->k.gpt * rep : 0)) * 4, 128);
+  const DecLayout L = dec_layout(D, rep, C->k.bits, C->k.axis, C->k.whole, C->k.gpt, C->k.meta_bytes, C->v.bits,
+                                 C->v.axis, C->v.whole, C->v.gpt, C->v.meta_bytes);
+  a.st_kc = L.st_kc;
+  a.st_km = L.st_km;
+  a.st_vc = L.st_vc;
+  a.st_vm = L.st_vm;
+  a.stage_bytes = L.stage_bytes;
+  a.lg_nstages = L.lg_ns;
+  a.barea_bytes = L.barea_bytes;
+  a.canon_k = L.canon_k;
+  a.canon_v = L.canon_v;
+  a.stage_off = L.stage_off;
+  a.warp_bytes = L.warp_bytes;
+  a.head_bytes = L.head_bytes;
   P->smem = (size_t)a.head_bytes + (size_t)kWarps * a.warp_bytes;
-  if (!pick_kernel(D, r8, C->v.axis)) return cudaErrorInvalidValue;
+  if (!C->dec_fn) return cudaErrorInvalidValue;
   *occ_out = C->dec_occ;
   return cudaSuccess;
 }
 
 cudaError_t decode_setup(kvq_cache* C) {
+  void* fn = C->generic_decode ? nullptr : decode_kernel_fast(C);
+  if (!fn) fn = pick_kernel(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
+  if (!fn) return cudaErrorInvalidValue;
+  C->dec_fn = fn;
   Plan P;
   int occ = 1;
   cudaError_t e = make_plan(C, 0, &P, &occ);
   if (e != cudaSuccess) return e;
-  void* fn = pick_kernel(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
   if (P.smem > 227 * 1024) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.smem);
   if (e != cudaSuccess) return e;
@@ -148,10 +165,9 @@ cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, flo
   a.q_f32 = q_f32;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = out;
-  void* fn = pick_kernel(cfg.head_dim, cfg.q_heads / cfg.kv_heads == 8, C->v.axis);
   dim3 grid(nch, cfg.kv_heads, cfg.batch);
   void* args[] = {&a};
-  e = cudaLaunchKernel(fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
+  e = cudaLaunchKernel(C->dec_fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
   ++*launches;
   return e;
 }
@@ -184,10 +200,9 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   a.q_f32 = q_f32;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = out;
-  void* fn = pick_kernel(cfg.head_dim, cfg.q_heads / cfg.kv_heads == 8, C->v.axis);
   dim3 grid(nch, cfg.kv_heads, cfg.batch);
   void* args[] = {&a};
-  e = cudaLaunchKernel(fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
+  e = cudaLaunchKernel(C->dec_fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
   ++*launches;
   return e;
 }

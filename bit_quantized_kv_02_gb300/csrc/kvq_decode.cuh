@@ -8,14 +8,16 @@
 //
 // Per 16-token tile a warp:
 //   1. waits for its stage: packed codes + metadata copied global -> shared by
-//      the TMA engine (cp.async.bulk, mbarrier completion, bounded waits);
+//      the TMA engine (cp.async.bulk, mbarrier completion, bounded waits), and
+//      turns the stage's metadata into fp32 (step, folded zero) pairs once;
 //   2. QK: converts the key codes of each 16-channel chunk to exact fp16
-//      operands in registers (rotate + one LOP3 per code pair: the code lands
-//      in the top mantissa bits of an fp16 whose exponent makes its value
-//      2^B + code) and runs mma.sync m16n8k16 against the query split into
-//      fp16 hi + lo parts (~22-bit operand, fp32 accumulation); scales, zero
-//      points and the 2^B offset are folded into the query (per-channel keys)
-//      or applied to the fp32 accumulators (per-token keys);
+//      operands in registers (one rotate + one LOP3 per code pair and bit
+//      plane: the code lands in the top mantissa bits of an fp16 whose
+//      exponent makes its value 2^B + code) and runs mma.sync m16n8k16 against
+//      the query split into fp16 hi + lo parts (~22-bit operand, fp32
+//      accumulation); steps, zero points and the 2^B offset are folded into
+//      the query (per-channel keys) or applied to the fp32 accumulators
+//      (per-token keys);
 //   3. online softmax in base 2 (fp32);
 //   4. PV: converts the value codes the same way (fragment rows = channels,
 //      columns = tokens) and runs mma.sync against the probabilities, split
@@ -73,15 +75,32 @@ __device__ __forceinline__ void convert_chunk(const uint32_t* tile, int lane, in
   }
 }
 
-// per-tensor metadata entry -> (zero', step) with zero' = zero - 2^B step (asym) or the
-// symmetric equivalent: the value is step * (2^B + code) + zero'
-__device__ __forceinline__ void meta_fold(const char* m, int idx, const TensorLayout& L, float* zf, float* st) {
-  float z, s;
-  load_meta(m, idx, L.meta_f32, L.sym, &z, &s);
-  const float off = (float)(1 << L.bits);
-  if (L.sym) z = -s * (float)(1 << (L.bits - 1));
-  *st = s;
-  *zf = z - off * s;
+template <int D>
+__device__ __forceinline__ void convert_dispatch(int bits, const uint32_t* tile, int lane, int j, uint32_t a[4]) {
+  switch (bits) {
+    case 2: convert_chunk<2, D>(tile, lane, j, a); break;
+    case 3: convert_chunk<3, D>(tile, lane, j, a); break;
+    case 4: convert_chunk<4, D>(tile, lane, j, a); break;
+    case 5: convert_chunk<5, D>(tile, lane, j, a); break;
+    case 6: convert_chunk<6, D>(tile, lane, j, a); break;
+    case 7: convert_chunk<7, D>(tile, lane, j, a); break;
+    default: convert_chunk<8, D>(tile, lane, j, a); break;
+  }
+}
+
+// Stored metadata entries [0, n) -> fp32 (step * post_scale, zero') with
+// zero' = zero - 2^B step (symmetric: zero = -2^(B-1) step), so that a value is
+// step * (2^B + code) + zero'.  One warp, entries strided over the lanes.
+__device__ __forceinline__ void canon_meta(const char* src, int n, int bits, int sym, int meta_f32, float post_scale,
+                                           float2* dst, int lane) {
+  const float off = (float)(1 << bits);
+  const float soff = 0.5f * off;
+  for (int i = lane; i < n; i += 32) {
+    float z, s;
+    load_meta(src, i, meta_f32, sym, &z, &s);
+    if (sym) z = -s * soff;
+    dst[i] = make_float2(s * post_scale, z - off * s);
+  }
 }
 
 template <bool R8>
@@ -93,181 +112,273 @@ struct Slots {
 
 // -------------------------------------------------- query operand build ---
 
-// Build the fragment-ordered QK B operand of one warp for a set of channel
-// scales (per-channel keys: this group's steps; per-token keys / fp16 tail:
-// unit scales), with the power-of-two normalisation E and the bias
-// sum_c q_c zero'_c per query.  Values (rho >= rep) stay zero.
+// Fragment-ordered QK B operand of one warp: q * s_c (kc = canonical
+// per-channel key metadata of the current group) or q (kc == null), scaled by
+// 2^E (E returned) and split into fp16 hi + lo; bias[rho] = sum_c q_c zero'_c.
+// Only valid query columns are written; the rest of barea stays zero.
 template <int D, bool R8>
-__device__ void build_qb(const float* qs, int rep, const char* kmeta_grp, const TensorLayout& K, bool unit,
-                         uint32_t* barea, float* bias, int* Eout) {
-  const int lane = threadIdx.x & 31;
-  // pass 1: max |q * s|
-  float mx = 0.0f;
-  for (int i = lane; i < rep * D; i += 32) {
-    int rho = i / D, c = i % D;
-    float s = 1.0f, z = 0.0f;
-    if (!unit) meta_fold(kmeta_grp, c, K, &z, &s);
-    mx = fmaxf(mx, fabsf(qs[rho * D + c] * s));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const int E = norm_exp(mx);
+__device__ __forceinline__ void build_qb(const float* qs, int rep, const float2* kc, uint32_t* barea, float* bias,
+                                         int E, int lane) {
   const float sc = exp2i(E);
-  // pass 2: channel pairs -> hi/lo fp16 pairs scattered to fragment positions
-  float bsum[8];
+  for (int rho = 0; rho < rep; ++rho) {
+    float bacc = 0.0f;
 #pragma unroll
-  for (int r = 0; r < 8; ++r) bsum[r] = 0.0f;
-  for (int i = lane; i < rep * (D / 2); i += 32) {
-    int rho = i / (D / 2), c = 2 * (i % (D / 2));
-    float s0 = 1.0f, z0 = 0.0f, s1 = 1.0f, z1 = 0.0f;
-    if (!unit) {
-      meta_fold(kmeta_grp, c, K, &z0, &s0);
-      meta_fold(kmeta_grp, c + 1, K, &z1, &s1);
+    for (int it = 0; it < D / 64; ++it) {
+      const int c = 2 * (lane + 32 * it);
+      const float2 q2 = *reinterpret_cast<const float2*>(qs + rho * D + c);
+      float s0 = sc, s1 = sc;
+      if (kc) {
+        const float4 m = *reinterpret_cast<const float4*>(kc + c);
+        s0 = m.x * sc;
+        s1 = m.z * sc;
+        bacc += q2.x * m.y + q2.y * m.w;
+      }
+      const float v0 = q2.x * s0, v1 = q2.y * s1;
+      const __half2 hh = __floats2half2_rn(v0, v1);
+      const float2 hf = __half22float2(hh);
+      const __half2 ll = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+      const int j = c >> 4, cc = c & 15, ttig = (cc & 7) >> 1, breg = cc >> 3;
+      if (!R8) {
+        barea[(j * 32 + 4 * (2 * rho) + ttig) * 2 + breg] = *reinterpret_cast<const uint32_t*>(&hh);
+        barea[(j * 32 + 4 * (2 * rho + 1) + ttig) * 2 + breg] = *reinterpret_cast<const uint32_t*>(&ll);
+      } else {
+        barea[((2 * j) * 32 + 4 * rho + ttig) * 2 + breg] = *reinterpret_cast<const uint32_t*>(&hh);
+        barea[((2 * j + 1) * 32 + 4 * rho + ttig) * 2 + breg] = *reinterpret_cast<const uint32_t*>(&ll);
+      }
     }
-    float q0 = qs[rho * D + c], q1 = qs[rho * D + c + 1];
-    float v0 = q0 * s0 * sc, v1 = q1 * s1 * sc;
-    __half h0, l0, h1, l1;
-    split_hl(v0, &h0, &l0);
-    split_hl(v1, &h1, &l1);
-    if (!unit) {
+    if (kc) {
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
-        if (r == rho) bsum[r] += q0 * z0 + q1 * z1;
-    }
-    // fragment position of channel pair (c, c+1): chunk j, tig, b0/b1
-    int j = c >> 4, cc = c & 15, tig = (cc & 7) >> 1, breg = cc >> 3;
-    if (!R8) {
-      int ghi = 2 * rho, glo = 2 * rho + 1;
-      barea[(j * 32 + 4 * ghi + tig) * 2 + breg] = pack_h2(h0, h1);
-      barea[(j * 32 + 4 * glo + tig) * 2 + breg] = pack_h2(l0, l1);
-    } else {
-      barea[((j * 2 + 0) * 32 + 4 * rho + tig) * 2 + breg] = pack_h2(h0, h1);
-      barea[((j * 2 + 1) * 32 + 4 * rho + tig) * 2 + breg] = pack_h2(l0, l1);
-    }
-  }
-  if (!unit) {
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      float v = bsum[r];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0 && r < rep) bias[r] = v;
+      for (int o = 16; o > 0; o >>= 1) bacc += __shfl_xor_sync(0xffffffffu, bacc, o);
+      if (lane == 0) bias[rho] = bacc;
     }
   }
-  *Eout = E;
   __syncwarp();
 }
 
+template <int V>
+struct IntC {
+  static constexpr int value = V;
+};
+
+// ------------------------------------------------------ configurations ---
+
+// Runtime configuration: every format field comes from the launch arguments
+// (the generic kernel, any format the C ABI accepts).
+struct DynCfg {
+  __device__ static int rep(const DecodeArgs& a) { return a.rep; }
+  __device__ static int kbits(const DecodeArgs& a) { return a.K.bits; }
+  __device__ static int ksym(const DecodeArgs& a) { return a.K.sym; }
+  __device__ static int kf32(const DecodeArgs& a) { return a.K.meta_f32; }
+  __device__ static int kwhole(const DecodeArgs& a) { return a.K.whole; }
+  __device__ static bool ktok(const DecodeArgs& a) { return a.K.axis == 0; }
+  __device__ static int kgpt(const DecodeArgs& a) { return a.K.gpt; }
+  __device__ static int klg(const DecodeArgs& a) { return a.K.lg_group; }
+  __device__ static int kG(const DecodeArgs& a) { return a.K.group; }
+  __device__ static int kmb(const DecodeArgs& a) { return a.K.meta_bytes; }
+  __device__ static int vbits(const DecodeArgs& a) { return a.V.bits; }
+  __device__ static int vsym(const DecodeArgs& a) { return a.V.sym; }
+  __device__ static int vf32(const DecodeArgs& a) { return a.V.meta_f32; }
+  __device__ static int vwhole(const DecodeArgs& a) { return a.V.whole; }
+  __device__ static int vgpt(const DecodeArgs& a) { return a.V.gpt; }
+  __device__ static int vlg(const DecodeArgs& a) { return a.V.lg_group; }
+  __device__ static int vG(const DecodeArgs& a) { return a.V.group; }
+  __device__ static int vmb(const DecodeArgs& a) { return a.V.meta_bytes; }
+  __device__ static int kc_bytes(const DecodeArgs& a) { return a.K.tile_bytes; }
+  __device__ static int vc_bytes(const DecodeArgs& a) { return a.V.tile_bytes; }
+  __device__ static int km_bytes(const DecodeArgs& a) { return a.K.mtile_bytes; }
+  __device__ static int vm_bytes(const DecodeArgs& a) { return a.V.mtile_bytes; }
+  __device__ static int st_kc(const DecodeArgs& a) { return a.st_kc; }
+  __device__ static int st_km(const DecodeArgs& a) { return a.st_km; }
+  __device__ static int st_vc(const DecodeArgs& a) { return a.st_vc; }
+  __device__ static int st_vm(const DecodeArgs& a) { return a.st_vm; }
+  __device__ static int stage_bytes(const DecodeArgs& a) { return a.stage_bytes; }
+  __device__ static int lg_ns(const DecodeArgs& a) { return a.lg_nstages; }
+  __device__ static int barea_bytes(const DecodeArgs& a) { return a.barea_bytes; }
+  __device__ static int canon_k(const DecodeArgs& a) { return a.canon_k; }
+  __device__ static int canon_v(const DecodeArgs& a) { return a.canon_v; }
+  __device__ static int stage_off(const DecodeArgs& a) { return a.stage_off; }
+  __device__ static int warp_bytes(const DecodeArgs& a) { return a.warp_bytes; }
+  __device__ static int head_bytes(const DecodeArgs& a) { return a.head_bytes; }
+};
+
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
+
+// Compile-time configuration (fp16 metadata, no whole-vector groups): every
+// format field and shared-memory offset is a constant, so index arithmetic,
+// format branches and group bookkeeping fold away.
+template <int D, int REP, int KB, int KAX, int KG, int KSYM, int VB, int VAX, int VG, int VSYM>
+struct StatCfg {
+  static constexpr int KGPT = KAX == 0 ? D / KG : 0, VGPT = VAX == 0 ? D / VG : 0;
+  static constexpr int KMB = KSYM ? 2 : 4, VMB = VSYM ? 2 : 4;
+  static constexpr DecLayout L = dec_layout(D, REP, KB, KAX, 0, KGPT, KMB, VB, VAX, 0, VGPT, VMB);
+  __device__ static constexpr int rep(const DecodeArgs&) { return REP; }
+  __device__ static constexpr int kbits(const DecodeArgs&) { return KB; }
+  __device__ static constexpr int ksym(const DecodeArgs&) { return KSYM; }
+  __device__ static constexpr int kf32(const DecodeArgs&) { return 0; }
+  __device__ static constexpr int kwhole(const DecodeArgs&) { return 0; }
+  __device__ static constexpr bool ktok(const DecodeArgs&) { return KAX == 0; }
+  __device__ static constexpr int kgpt(const DecodeArgs&) { return KGPT; }
+  __device__ static constexpr int klg(const DecodeArgs&) { return ilog2(KG); }
+  __device__ static constexpr int kG(const DecodeArgs&) { return KG; }
+  __device__ static constexpr int kmb(const DecodeArgs&) { return KMB; }
+  __device__ static constexpr int vbits(const DecodeArgs&) { return VB; }
+  __device__ static constexpr int vsym(const DecodeArgs&) { return VSYM; }
+  __device__ static constexpr int vf32(const DecodeArgs&) { return 0; }
+  __device__ static constexpr int vwhole(const DecodeArgs&) { return 0; }
+  __device__ static constexpr int vgpt(const DecodeArgs&) { return VGPT; }
+  __device__ static constexpr int vlg(const DecodeArgs&) { return ilog2(VG); }
+  __device__ static constexpr int vG(const DecodeArgs&) { return VG; }
+  __device__ static constexpr int vmb(const DecodeArgs&) { return VMB; }
+  __device__ static constexpr int kc_bytes(const DecodeArgs&) { return L.kc_bytes; }
+  __device__ static constexpr int vc_bytes(const DecodeArgs&) { return L.vc_bytes; }
+  __device__ static constexpr int km_bytes(const DecodeArgs&) { return L.km_bytes; }
+  __device__ static constexpr int vm_bytes(const DecodeArgs&) { return L.vm_bytes; }
+  __device__ static constexpr int st_kc(const DecodeArgs&) { return L.st_kc; }
+  __device__ static constexpr int st_km(const DecodeArgs&) { return L.st_km; }
+  __device__ static constexpr int st_vc(const DecodeArgs&) { return L.st_vc; }
+  __device__ static constexpr int st_vm(const DecodeArgs&) { return L.st_vm; }
+  __device__ static constexpr int stage_bytes(const DecodeArgs&) { return L.stage_bytes; }
+  __device__ static constexpr int lg_ns(const DecodeArgs&) { return L.lg_ns; }
+  __device__ static constexpr int barea_bytes(const DecodeArgs&) { return L.barea_bytes; }
+  __device__ static constexpr int canon_k(const DecodeArgs&) { return L.canon_k; }
+  __device__ static constexpr int canon_v(const DecodeArgs&) { return L.canon_v; }
+  __device__ static constexpr int stage_off(const DecodeArgs&) { return L.stage_off; }
+  __device__ static constexpr int warp_bytes(const DecodeArgs&) { return L.warp_bytes; }
+  __device__ static constexpr int head_bytes(const DecodeArgs&) { return L.head_bytes; }
+};
+
 // --------------------------------------------------------------- kernel ----
 
-template <int D, bool R8, int VAXIS>
-__global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
+// resident CTAs per SM the register budget is sized for
+__host__ __device__ constexpr int decode_min_blocks(int D) { return D == 64 ? 5 : (D == 128 ? 3 : 2); }
+
+template <int D, bool R8, int VAXIS, class CFG>
+__global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  constexpr int NCH = D / 16;  // 16-channel chunks / m-tiles
+  constexpr int NCH = D / 16;                // 16-channel chunks / m-tiles
+  constexpr int NB = R8 ? 2 : 1;             // B operands per chunk (hi/lo split over two MMAs)
+  constexpr bool BREG = NCH * 2 * NB <= 16;  // query operand kept in registers
+  constexpr int GV_MAX = D / 32;             // per-token value groups per head row (group >= 32)
   using SL = Slots<R8>;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
-  const int rep = a.rep;
+  const int rep = CFG::rep(a), H = a.H, S = a.S;
   const int n = a.lens[b];
-  const int nchunks = (n + a.S - 1) / a.S;
+  const int nchunks = (n + S - 1) / S;
   const int hq0 = h * rep;
   if (n == 0) {
     if (chunk == 0)
-      for (int i = threadIdx.x; i < rep * D; i += blockDim.x) a.out[((long)b * a.H * rep + hq0) * D + i] = 0.0f;
+      for (int i = threadIdx.x; i < rep * D; i += blockDim.x) a.out[((long)b * H * rep + hq0) * D + i] = 0.0f;
     return;
   }
   if (chunk >= nchunks) return;
 
+  // ---- tensor formats (constants in a compile-time configuration)
+  const int kbits = CFG::kbits(a), ksym = CFG::ksym(a), kf32 = CFG::kf32(a), kwhole = CFG::kwhole(a);
+  const bool k_token = CFG::ktok(a);
+  const int kgpt = CFG::kgpt(a), k_lgG = CFG::klg(a), kG = CFG::kG(a);
+  const int vbits = CFG::vbits(a), vsym = CFG::vsym(a), vf32 = CFG::vf32(a), vwhole = CFG::vwhole(a);
+  const int vgpt = CFG::vgpt(a), v_lgG = CFG::vlg(a), vG = CFG::vG(a);
+  const int kmb = CFG::kmb(a), vmb = CFG::vmb(a);
+  const int kc_bytes = CFG::kc_bytes(a), vc_bytes = CFG::vc_bytes(a);
+  const int km_bytes = CFG::km_bytes(a), vm_bytes = CFG::vm_bytes(a);
+  const int st_kc = CFG::st_kc(a), st_km = CFG::st_km(a), st_vc = CFG::st_vc(a), st_vm = CFG::st_vm(a);
+  const int stage_bytes = CFG::stage_bytes(a), lg_ns = CFG::lg_ns(a), ns = 1 << lg_ns;
+  const int tcap = a.tcap, ntiles = a.ntiles;
+
   // ---- shared memory carve-up
-  float* qs = reinterpret_cast<float*>(smem);          // [rep][D] q * scale * log2(e)
-  float* qg = qs + rep * D;                              // [gpt_k][rep] per-token key group sums of q
-  unsigned char* wbase = smem + a.head_bytes + warp * a.warp_bytes;
-  uint32_t* barea = reinterpret_cast<uint32_t*>(wbase);  // QK B operand
-  float* wbias = reinterpret_cast<float*>(wbase + a.barea_bytes);  // [8] per-channel key bias
-  unsigned char* stages = wbase + a.barea_bytes + 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + a.nstages * a.stage_bytes);
+  float* qs = reinterpret_cast<float*>(smem);  // [rep][D] q * scale * log2(e)
+  float* qg = qs + rep * D;                     // [gpt_k][rep] per-token key group sums of q
+  unsigned char* wbase = smem + CFG::head_bytes(a) + warp * CFG::warp_bytes(a);
+  uint32_t* barea = reinterpret_cast<uint32_t*>(wbase);                    // QK B operand
+  float2* canK = reinterpret_cast<float2*>(wbase + CFG::barea_bytes(a));  // canonical key metadata
+  float2* canV = canK + CFG::canon_k(a);                                   // canonical value metadata
+  float* wbias = reinterpret_cast<float*>(canV + CFG::canon_v(a));         // [8] per-channel key bias
+  unsigned char* stages = wbase + CFG::stage_off(a);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (stage_bytes << lg_ns));
 
   for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
-    const long qi = ((long)b * a.H * rep + hq0) * D + i;
+    const long qi = ((long)b * H * rep + hq0) * D + i;
     qs[i] = (a.q_f32 ? reinterpret_cast<const float*>(a.q)[qi] : __half2float(reinterpret_cast<const __half*>(a.q)[qi])) *
             a.scale_log2;
   }
-  const int gpt_k = a.K.gpt;
-  const bool k_token = a.K.axis == 0, k_whole = a.K.whole;
   __syncthreads();
   if (k_token) {
-    const int Gk = k_whole ? D : a.K.group;  // within one head a whole-vector group spans all D channels
-    for (int i = threadIdx.x; i < gpt_k * rep; i += blockDim.x) {
-      int jg = i / rep, rho = i % rep;
+    const int Gk = kwhole ? D : kG;  // within one head a whole-vector group spans all D channels
+    for (int i = threadIdx.x; i < kgpt * rep; i += blockDim.x) {
+      const int jg = i / rep, rho = i % rep;
       float s = 0.0f;
       for (int c = jg * Gk; c < (jg + 1) * Gk; ++c) s += qs[rho * D + c];
       qg[jg * rep + rho] = s;
     }
   }
-  // zero this warp's B operand area (unused query columns must stay zero)
-  for (int i = lane; i < a.barea_bytes / 4; i += 32) barea[i] = 0u;
+  for (int i = lane; i < CFG::barea_bytes(a) / 4; i += 32) barea[i] = 0u;
+  if (lane < 8) wbias[lane] = 0.0f;
   if (lane == 0)
-    for (int s = 0; s < a.nstages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < ns; ++s) mbar_init(&bars[s], 1);
   fence_mbar_init();
   __syncthreads();
 
-  // ---- this warp's token range
-  const int w0 = chunk * a.S + warp * a.Sw;
+  // ---- this warp's token range and its copy sources
+  const int w0 = chunk * S + warp * a.Sw;
   const int w1 = min(w0 + a.Sw, n);
   const int ntl = w1 > w0 ? (w1 - w0 + kTile - 1) / kTile : 0;
-  const int sealed_k = a.K.axis == 1 ? (n / a.K.group) * a.K.group : n;
-  const int sealed_v = a.V.axis == 1 ? (n / a.V.group) * a.V.group : n;
-  const long bh = (long)b * a.H + h;
-  const char* kcodes = a.base + a.K.codes_off + a.layer * a.K.codes_layer + bh * a.ntiles * (long)a.kc_bytes;
-  const char* vcodes = a.base + a.V.codes_off + a.layer * a.V.codes_layer + bh * a.ntiles * (long)a.vc_bytes;
-  const char* kmeta = a.base + a.K.meta_off + a.layer * a.K.meta_layer;
-  const char* vmeta = a.base + a.V.meta_off + a.layer * a.V.meta_layer;
-  const __half* ktail = reinterpret_cast<const __half*>(a.base + a.K.tail_off + a.layer * a.K.tail_layer) +
-                        bh * a.K.group * D;
-  const __half* vtail = reinterpret_cast<const __half*>(a.base + a.V.tail_off + a.layer * a.V.tail_layer) +
-                        bh * a.V.group * D;
-
-  auto meta_src = [&](const TensorLayout& L, const char* mbase, int t0, int per_tile_bytes) -> const char* {
-    long idx;
-    if (L.whole) idx = (long)b * a.tcap + t0;
-    else idx = (bh * a.tcap + t0) * L.gpt;
-    (void)per_tile_bytes;
-    return mbase + idx * L.meta_bytes;
-  };
+  const int sealed_k = k_token ? n : ((n >> k_lgG) << k_lgG);
+  const int sealed_v = VAXIS == 0 ? n : ((n >> v_lgG) << v_lgG);
+  const long bh = (long)b * H + h;
+  const char* kc_src = a.K.codes + (bh * ntiles + (w0 >> 4)) * (long)kc_bytes;
+  const char* vc_src = a.V.codes + (bh * ntiles + (w0 >> 4)) * (long)vc_bytes;
+  // per-token metadata of the range's first tile (whole vector: per sequence), or its first per-channel group
+  const char* km_src = k_token ? a.K.meta + (kwhole ? ((long)b * tcap + w0) : ((bh * tcap + w0) * kgpt)) * kmb
+                               : a.K.meta + ((bh * (tcap >> k_lgG) + (w0 >> k_lgG)) * D) * kmb;
+  const char* vm_src = VAXIS == 0 ? a.V.meta + (vwhole ? ((long)b * tcap + w0) : ((bh * tcap + w0) * vgpt)) * vmb
+                                  : a.V.meta + ((bh * (tcap >> v_lgG) + (w0 >> v_lgG)) * D) * vmb;
+  const __half* ktail = a.K.tail + bh * kG * D;
+  const __half* vtail = a.V.tail + bh * vG * D;
+  const int kgmask = k_token ? 0 : kG - 1;
+  const int vgmask = VAXIS == 0 ? 0 : vG - 1;
 
   auto issue = [&](int i) {
-    const int s = i % a.nstages;
+    const int s = i & (ns - 1);
     const int t0 = w0 + i * kTile;
-    unsigned char* st = stages + s * a.stage_bytes;
-    uint32_t bytes = 0;
+    unsigned char* st = stages + s * stage_bytes;
     const bool kp = t0 < sealed_k, vp = t0 < sealed_v;
-    const bool kgrp = kp && a.K.axis == 1 && (t0 % a.K.group) == 0;
-    const bool vgrp = vp && a.V.axis == 1 && ((t0 + kTile) % a.V.group) == 0;
-    if (kp) bytes += a.kc_bytes + (a.K.axis == 1 ? (kgrp ? a.km_group_bytes : 0) : a.km_tile_bytes);
-    if (vp) bytes += a.vc_bytes + (a.V.axis == 1 ? (vgrp ? a.vm_group_bytes : 0) : a.vm_tile_bytes);
-    mbar_expect_tx(&bars[s], bytes);
+    uint32_t bytes = 0, kmb_i = 0, vmb_i = 0;
+    const char* kms = km_src;
+    const char* vms = vm_src;
     if (kp) {
-      bulk_g2s(st + a.st_kc, kcodes + (long)(t0 / kTile) * a.kc_bytes, a.kc_bytes, &bars[s]);
-      if (a.K.axis == 0) bulk_g2s(st + a.st_km, meta_src(a.K, kmeta, t0, a.km_tile_bytes), a.km_tile_bytes, &bars[s]);
-      else if (kgrp)
-        bulk_g2s(st + a.st_km, kmeta + ((bh * (a.tcap / a.K.group) + t0 / a.K.group) * D) * a.K.meta_bytes,
-                 a.km_group_bytes, &bars[s]);
+      if (k_token) {
+        kms += (long)i * km_bytes;
+        kmb_i = km_bytes;
+      } else if ((t0 & kgmask) == 0) {
+        kms += (long)((t0 - w0) >> k_lgG) * km_bytes;
+        kmb_i = km_bytes;
+      }
+      bytes += kc_bytes + kmb_i;
     }
     if (vp) {
-      bulk_g2s(st + a.st_vc, vcodes + (long)(t0 / kTile) * a.vc_bytes, a.vc_bytes, &bars[s]);
-      if (a.V.axis == 0) bulk_g2s(st + a.st_vm, meta_src(a.V, vmeta, t0, a.vm_tile_bytes), a.vm_tile_bytes, &bars[s]);
-      else if (vgrp)
-        bulk_g2s(st + a.st_vm, vmeta + ((bh * (a.tcap / a.V.group) + t0 / a.V.group) * D) * a.V.meta_bytes,
-                 a.vm_group_bytes, &bars[s]);
+      if (VAXIS == 0) {
+        vms += (long)i * vm_bytes;
+        vmb_i = vm_bytes;
+      } else if (((t0 + kTile) & vgmask) == 0) {
+        vms += (long)((t0 - w0) >> v_lgG) * vm_bytes;
+        vmb_i = vm_bytes;
+      }
+      bytes += vc_bytes + vmb_i;
     }
+    mbar_expect_tx(&bars[s], bytes);
+    if (kp) bulk_g2s(st + st_kc, kc_src + (long)i * kc_bytes, kc_bytes, &bars[s]);
+    if (kmb_i) bulk_g2s(st + st_km, kms, kmb_i, &bars[s]);
+    if (vp) bulk_g2s(st + st_vc, vc_src + (long)i * vc_bytes, vc_bytes, &bars[s]);
+    if (vmb_i) bulk_g2s(st + st_vm, vms, vmb_i, &bars[s]);
   };
 
   if (lane == 0)
-    for (int i = 0; i < min(ntl, a.nstages); ++i) issue(i);
+    for (int i = 0; i < min(ntl, ns); ++i) issue(i);
 
   // ---- per-warp state
-  float m_run[SL::N], l_run[SL::N];  // per slot (slots with equal rho hold equal m)
+  float m_run[SL::N], l_run[SL::N];
 #pragma unroll
   for (int s = 0; s < SL::N; ++s) {
     m_run[s] = -INFINITY;
@@ -278,11 +389,9 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
   for (int j = 0; j < NCH; ++j)
 #pragma unroll
     for (int r = 0; r < 4; ++r) O[j][r] = 0.0f;
-  // per-token values: zero-point sums per group and slot-query; per-channel values: group accumulators
-  constexpr int GV_MAX = D / 32;
-  float Zs[GV_MAX][SL::N];
+  float Zs[VAXIS == 0 ? GV_MAX : 1][SL::N];
 #pragma unroll
-  for (int jg = 0; jg < GV_MAX; ++jg)
+  for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
 #pragma unroll
     for (int s = 0; s < SL::N; ++s) Zs[jg][s] = 0.0f;
   float Og[VAXIS == 1 ? NCH : 1][4];
@@ -294,147 +403,223 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
 #pragma unroll
   for (int s = 0; s < SL::N; ++s) Pg[s] = 0.0f;
 
-  int Eq = 0;
-  bool qb_unit = false;  // barea holds plain q (per-token keys or key tail)
+  uint32_t breg[BREG ? NCH * 2 * NB : 1];
+  auto load_b = [&]() {
+    if (BREG) {
+#pragma unroll
+      for (int j = 0; j < NCH; ++j)
+#pragma unroll
+        for (int hl2 = 0; hl2 < NB; ++hl2) {
+          const uint2 v = reinterpret_cast<const uint2*>(barea)[(j * NB + hl2) * 32 + lane];
+          breg[BREG ? (j * NB + hl2) * 2 : 0] = v.x;
+          breg[BREG ? (j * NB + hl2) * 2 + 1 : 0] = v.y;
+        }
+    }
+  };
+  // query operand normalisation: q * step * 2^E stays below 2^15 for every key
+  // group (the largest stored key step of this sequence/head bounds the steps)
+  float qmax = 0.0f;
+  for (int i = lane; i < rep * D; i += 32) qmax = fmaxf(qmax, fabsf(qs[i]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+  const int E_unit = norm_exp(qmax);
+  const int E_chan = k_token ? E_unit : norm_exp(qmax * __uint_as_float(a.smax_k[(long)b * H + h]));
+  int Ek = E_unit;
+  bool qb_unit = false;
   if (k_token) {
-    build_qb<D, R8>(qs, rep, nullptr, a.K, true, barea, wbias, &Eq);
+    build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, lane);
     qb_unit = true;
+    load_b();
   }
-  const float inv_eq_tok = exp2i(-Eq);
-  int E_v = 0;
-  if (a.V.axis == 0) {
-    float smax = __uint_as_float(a.smax_v[bh]);
-    E_v = norm_exp(smax);
-  }
+  // value step normalisation: every folded p * step lies below 2^15
+  const int E_v = VAXIS == 0 ? norm_exp(__uint_as_float(a.smax_v[bh])) : 0;
   const float sc_v = exp2i(E_v), inv_sc_v = exp2i(-E_v);
-  int Ek = Eq;
+  const int hl = g & 1;
+  // per-lane rows into the canonical metadata
+  const int gs_k = kwhole ? 1 : kgpt, gs_v = vwhole ? 1 : vgpt;
+  const int cpgk = k_token ? (kwhole ? NCH : (kG >> 4)) : NCH;  // chunks per key group (per-token keys)
+  const int cpgv = VAXIS == 0 ? (vwhole ? NCH : (vG >> 4)) : NCH;
+  const int lg_cpgk = 31 - __clz(cpgk), lg_cpgv = 31 - __clz(cpgv);
+  const float2* ck_row0 = canK + g * gs_k;
+  const float2* ck_row1 = canK + (g + 8) * gs_k;
+  const float2* cv_row0 = canV + g * gs_v;  // score-owner rows (zero-point sums)
+  const float2* cv_row1 = canV + (g + 8) * gs_v;
+  const int tk0 = 2 * tig;
+  const float2* cv_t0 = canV + tk0 * gs_v;  // B-operand tokens 2tig, 2tig+1, 2tig+8, 2tig+9
+  const float2* cv_t1 = canV + (tk0 + 1) * gs_v;
+  const float2* cv_t2 = canV + (tk0 + 8) * gs_v;
+  const float2* cv_t3 = canV + (tk0 + 9) * gs_v;
   bool failed = false;
 
   for (int i = 0; i < ntl; ++i) {
-    const int s = i % a.nstages;
+    const int s = i & (ns - 1);
     const int t0 = w0 + i * kTile;
-    if (!failed && !mbar_wait_bounded(&bars[s], (uint32_t)((i / a.nstages) & 1), a.err)) failed = true;
-    if (failed) break;
-    const unsigned char* st = stages + s * a.stage_bytes;
+    if (!mbar_wait_bounded(&bars[s], (uint32_t)((i >> lg_ns) & 1), a.err)) {
+      failed = true;
+      break;
+    }
+    const unsigned char* st = stages + s * stage_bytes;
     const bool kp = t0 < sealed_k, vp = t0 < sealed_v;
+    const bool vflush = VAXIS == 1 && vp && ((t0 + kTile) & vgmask) == 0;
+
+    // ---- metadata of this stage -> canonical fp32 pairs
+    if (kp) {
+      if (k_token) {
+        canon_meta(reinterpret_cast<const char*>(st + st_km), kTile * gs_k, kbits, ksym, kf32, exp2i(-Ek), canK, lane);
+      } else if ((t0 & kgmask) == 0) {
+        canon_meta(reinterpret_cast<const char*>(st + st_km), D, kbits, ksym, kf32, 1.0f, canK, lane);
+        __syncwarp();
+        Ek = E_chan;
+        build_qb<D, R8>(qs, rep, canK, barea, wbias, E_chan, lane);
+        qb_unit = false;
+        load_b();
+      }
+    } else if (!qb_unit) {
+      Ek = E_unit;
+      build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, lane);
+      qb_unit = true;
+      load_b();
+    }
+    if (vp) {
+      if (VAXIS == 0)
+        canon_meta(reinterpret_cast<const char*>(st + st_vm), kTile * gs_v, vbits, vsym, vf32, sc_v, canV, lane);
+      else if (vflush)
+        canon_meta(reinterpret_cast<const char*>(st + st_vm), D, vbits, vsym, vf32, 1.0f, canV, lane);
+    }
+    __syncwarp();
 
     // ------------------------------------------------------------ QK ----
     float score[SL::N];
 #pragma unroll
     for (int q = 0; q < SL::N; ++q) score[q] = 0.0f;
-    if (kp && a.K.axis == 1 && (t0 % a.K.group) == 0) {
-      build_qb<D, R8>(qs, rep, reinterpret_cast<const char*>(st + a.st_km), a.K, false, barea, wbias, &Ek);
-      qb_unit = false;
-    } else if (!kp && !qb_unit) {
-      build_qb<D, R8>(qs, rep, nullptr, a.K, true, barea, wbias, &Ek);
-      qb_unit = true;
-    }
     {
       float C[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t* ktile = reinterpret_cast<const uint32_t*>(st + a.st_kc);
-      const int cpg = k_token ? (k_whole ? NCH : a.K.group / 16) : NCH;
+      float C2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulation chain (odd chunks)
+      const uint32_t* ktile = reinterpret_cast<const uint32_t*>(st + st_kc);
+      const bool ktok = kp && k_token;
       const float inv_e = exp2i(-Ek);
-      auto fold_group = [&](int jg) {
+      auto fold = [&](int jg) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) C[r] += C2[r];
 #pragma unroll
         for (int q = 0; q < SL::N; ++q) {
-          float v = R8 ? C[q] : (C[2 * q] + C[2 * q + 1]);
-          if (kp && k_token) {
-            const int row = g + 8 * SL::rh(q);
-            float zf, stp;
-            meta_fold(reinterpret_cast<const char*>(st + a.st_km), k_whole ? row : row * gpt_k + jg, a.K, &zf, &stp);
-            const int rho = SL::rho(q, tig);
-            const float qsum = rho < rep ? qg[jg * rep + rho] : 0.0f;
-            score[q] += stp * v * inv_e + zf * qsum;
+          const float v = R8 ? C[q] : (C[2 * q] + C[2 * q + 1]);
+          if (ktok) {
+            const float2 m = (SL::rh(q) ? ck_row1 : ck_row0)[jg];
+            const int rho = min(SL::rho(q, tig), rep - 1);
+            score[q] += m.x * v + m.y * qg[jg * rep + rho];
           } else if (kp) {
-            const int rho = SL::rho(q, tig);
-            score[q] += v * inv_e + (rho < rep ? wbias[rho] : 0.0f);
+            score[q] += v * inv_e + wbias[SL::rho(q, tig)];
           } else {
             score[q] += v * inv_e;
           }
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r) C[r] = 0.0f;
+        for (int r = 0; r < 4; ++r) {
+          C[r] = 0.0f;
+          C2[r] = 0.0f;
+        }
       };
+      auto mma_chunk = [&](int j, const uint32_t* A) {
 #pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        uint32_t A[4];
-        if (kp) {
-          switch (a.K.bits) {
-            case 2: convert_chunk<2, D>(ktile, lane, j, A); break;
-            case 3: convert_chunk<3, D>(ktile, lane, j, A); break;
-            case 4: convert_chunk<4, D>(ktile, lane, j, A); break;
-            case 5: convert_chunk<5, D>(ktile, lane, j, A); break;
-            case 6: convert_chunk<6, D>(ktile, lane, j, A); break;
-            case 7: convert_chunk<7, D>(ktile, lane, j, A); break;
-            default: convert_chunk<8, D>(ktile, lane, j, A); break;
+        for (int hl2 = 0; hl2 < NB; ++hl2) {
+          uint32_t b0, b1;
+          if (BREG) {
+            b0 = breg[BREG ? (j * NB + hl2) * 2 : 0];
+            b1 = breg[BREG ? (j * NB + hl2) * 2 + 1 : 0];
+          } else {
+            const uint2 v = reinterpret_cast<const uint2*>(barea)[(j * NB + hl2) * 32 + lane];
+            b0 = v.x;
+            b1 = v.y;
           }
-        } else {
+          if (j & 1) mma_16816(C2, A[0], A[1], A[2], A[3], b0, b1);
+          else mma_16816(C, A[0], A[1], A[2], A[3], b0, b1);
+        }
+      };
+      auto qk_packed = [&](auto kb) {
+        constexpr int KB = decltype(kb)::value;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          uint32_t A[4];
+          convert_chunk<KB, D>(ktile, lane, j, A);
+          mma_chunk(j, A);
+          if (ktok && ((j + 1) & (cpgk - 1)) == 0) fold(j >> lg_cpgk);
+        }
+      };
+      if (kp) {
+        switch (kbits) {
+          case 2: qk_packed(IntC<2>{}); break;
+          case 3: qk_packed(IntC<3>{}); break;
+          case 4: qk_packed(IntC<4>{}); break;
+          case 5: qk_packed(IntC<5>{}); break;
+          case 6: qk_packed(IntC<6>{}); break;
+          case 7: qk_packed(IntC<7>{}); break;
+          default: qk_packed(IntC<8>{}); break;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
           // fp16 tail rows: token row R = g + 8*rh, channels 16j + 2tig + 8*kh (+1)
           const __half* tb = ktail + (long)(t0 - sealed_k) * D + 16 * j + 2 * tig;
+          uint32_t A[4];
           A[0] = *reinterpret_cast<const uint32_t*>(tb + (long)g * D);
           A[1] = *reinterpret_cast<const uint32_t*>(tb + (long)(g + 8) * D);
           A[2] = *reinterpret_cast<const uint32_t*>(tb + (long)g * D + 8);
           A[3] = *reinterpret_cast<const uint32_t*>(tb + (long)(g + 8) * D + 8);
-        }
-        if (!R8) {
-          uint2 bb = reinterpret_cast<const uint2*>(barea)[j * 32 + lane];
-          mma_16816(C, A[0], A[1], A[2], A[3], bb.x, bb.y);
-        } else {
-          uint2 bh2 = reinterpret_cast<const uint2*>(barea)[(j * 2) * 32 + lane];
-          uint2 bl2 = reinterpret_cast<const uint2*>(barea)[(j * 2 + 1) * 32 + lane];
-          mma_16816(C, A[0], A[1], A[2], A[3], bh2.x, bh2.y);
-          mma_16816(C, A[0], A[1], A[2], A[3], bl2.x, bl2.y);
-        }
-        if (kp && k_token) {
-          if ((j + 1) % cpg == 0) fold_group(j / cpg);
+          mma_chunk(j, A);
         }
       }
-      if (!(kp && k_token)) fold_group(0);
+      if (!ktok) fold(0);
     }
 
     // --------------------------------------------------------- softmax --
     float p[SL::N];
     float alpha[SL::N];
     {
-      float tmax[SL::N];
+      if (t0 + kTile > w1) {  // partial last tile of the range
 #pragma unroll
-      for (int q = 0; q < SL::N; ++q) {
-        const int t = t0 + g + 8 * SL::rh(q);
-        const int rho = SL::rho(q, tig);
-        if (t >= w1 || rho >= rep) score[q] = -INFINITY;
-        tmax[q] = score[q];
+        for (int q = 0; q < SL::N; ++q)
+          if (t0 + g + 8 * SL::rh(q) >= w1) score[q] = -INFINITY;
       }
-      // combine the two row-halves of the same query, then across the 8 token rows
+      // the running max only moves when some score of the tile exceeds it
+      bool up = false;
 #pragma unroll
-      for (int q = 0; q < SL::N; ++q) {
-        const int q2 = R8 ? (q ^ 2) : (q ^ 1);
-        if (q < q2) {
-          float m2 = fmaxf(tmax[q], tmax[q2]);
-          tmax[q] = m2;
-          tmax[q2] = m2;
+      for (int q = 0; q < SL::N; ++q) up |= score[q] > m_run[q];
+      if (__any_sync(0xffffffffu, up)) {
+        float tmax[SL::N];
+#pragma unroll
+        for (int q = 0; q < SL::N; ++q) tmax[q] = score[q];
+#pragma unroll
+        for (int q = 0; q < SL::N; ++q) {
+          const int q2 = R8 ? (q ^ 2) : (q ^ 1);
+          if (q < q2) {
+            float m2 = fmaxf(tmax[q], tmax[q2]);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) m2 = fmaxf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+            tmax[q] = m2;
+            tmax[q2] = m2;
+          }
         }
+#pragma unroll
+        for (int q = 0; q < SL::N; ++q) {
+          const float mnew = fmaxf(m_run[q], tmax[q]);
+          alpha[q] = fast_exp2(m_run[q] - mnew);
+          m_run[q] = mnew;
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < SL::N; ++q) alpha[q] = 1.0f;
       }
 #pragma unroll
       for (int q = 0; q < SL::N; ++q) {
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) tmax[q] = fmaxf(tmax[q], __shfl_xor_sync(0xffffffffu, tmax[q], o));
-      }
-#pragma unroll
-      for (int q = 0; q < SL::N; ++q) {
-        const float mnew = fmaxf(m_run[q], tmax[q]);
-        alpha[q] = (mnew == -INFINITY) ? 1.0f : fast_exp2(m_run[q] - mnew);
-        p[q] = (mnew == -INFINITY) ? 0.0f : fast_exp2(score[q] - mnew);
-        m_run[q] = mnew;
+        p[q] = fast_exp2(score[q] - m_run[q]);
         l_run[q] = l_run[q] * alpha[q] + p[q];
       }
     }
-    // rescale accumulators: O columns of this thread belong to its slot queries
     {
-      // non-R8: columns (2tig, 2tig+1) = (rho = tig, hi/lo) -> alpha[0] (== alpha[1])
-      // R8    : columns (2tig, 2tig+1) = rho 2tig, 2tig+1   -> alpha[0], alpha[1]
+      // O columns of this thread: non-R8 (rho = tig, hi/lo), R8 (rho = 2tig, 2tig+1)
       const float a0 = alpha[0], a1 = R8 ? alpha[1] : alpha[0];
-      const bool need = (a0 != 1.0f) || (a1 != 1.0f);
-      if (__any_sync(0xffffffffu, need)) {
+      if (__any_sync(0xffffffffu, (a0 != 1.0f) || (a1 != 1.0f))) {
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           O[j][0] *= a0;
@@ -442,65 +627,56 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
           O[j][2] *= a0;
           O[j][3] *= a1;
           if (VAXIS == 1) {
-            Og[j][0] *= a0;
-            Og[j][1] *= a1;
-            Og[j][2] *= a0;
-            Og[j][3] *= a1;
+            Og[VAXIS == 1 ? j : 0][0] *= a0;
+            Og[VAXIS == 1 ? j : 0][1] *= a1;
+            Og[VAXIS == 1 ? j : 0][2] *= a0;
+            Og[VAXIS == 1 ? j : 0][3] *= a1;
           }
         }
 #pragma unroll
         for (int q = 0; q < SL::N; ++q) {
           Pg[q] *= alpha[q];
 #pragma unroll
-          for (int jg = 0; jg < GV_MAX; ++jg) Zs[jg][q] *= alpha[q];
+          for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg) Zs[jg][q] *= alpha[q];
         }
       }
     }
 
     // ------------------------------------------------------------ PV ----
     {
-      // gather p for the B operand: tokens 2tig, 2tig+1, 2tig+8, 2tig+9 of column n = g
+      // p of tokens 2tig, 2tig+1, 2tig+8, 2tig+9 for this lane's B column n = g
       float pv[4];
       {
         const int srcA = 8 * tig, srcB = 8 * tig + 4;
         if (!R8) {
           const int rho = g >> 1;
-          float x0 = __shfl_sync(0xffffffffu, p[0], srcA + (rho & 3));
-          float x1 = __shfl_sync(0xffffffffu, p[0], srcB + (rho & 3));
-          float x2 = __shfl_sync(0xffffffffu, p[1], srcA + (rho & 3));
-          float x3 = __shfl_sync(0xffffffffu, p[1], srcB + (rho & 3));
-          pv[0] = x0; pv[1] = x1; pv[2] = x2; pv[3] = x3;
+          pv[0] = __shfl_sync(0xffffffffu, p[0], srcA + rho);
+          pv[1] = __shfl_sync(0xffffffffu, p[0], srcB + rho);
+          pv[2] = __shfl_sync(0xffffffffu, p[1], srcA + rho);
+          pv[3] = __shfl_sync(0xffffffffu, p[1], srcB + rho);
         } else {
           const int src_t = g >> 1, par = g & 1;
-          float e0 = __shfl_sync(0xffffffffu, p[0], srcA + src_t);
-          float e1 = __shfl_sync(0xffffffffu, p[1], srcA + src_t);
-          float f0 = __shfl_sync(0xffffffffu, p[0], srcB + src_t);
-          float f1 = __shfl_sync(0xffffffffu, p[1], srcB + src_t);
-          float e2 = __shfl_sync(0xffffffffu, p[2], srcA + src_t);
-          float e3 = __shfl_sync(0xffffffffu, p[3], srcA + src_t);
-          float f2 = __shfl_sync(0xffffffffu, p[2], srcB + src_t);
-          float f3 = __shfl_sync(0xffffffffu, p[3], srcB + src_t);
+          const float e0 = __shfl_sync(0xffffffffu, p[0], srcA + src_t);
+          const float e1 = __shfl_sync(0xffffffffu, p[1], srcA + src_t);
+          const float f0 = __shfl_sync(0xffffffffu, p[0], srcB + src_t);
+          const float f1 = __shfl_sync(0xffffffffu, p[1], srcB + src_t);
+          const float e2 = __shfl_sync(0xffffffffu, p[2], srcA + src_t);
+          const float e3 = __shfl_sync(0xffffffffu, p[3], srcA + src_t);
+          const float f2 = __shfl_sync(0xffffffffu, p[2], srcB + src_t);
+          const float f3 = __shfl_sync(0xffffffffu, p[3], srcB + src_t);
           pv[0] = par ? e1 : e0;
           pv[1] = par ? f1 : f0;
           pv[2] = par ? e3 : e2;
           pv[3] = par ? f3 : f2;
         }
       }
-      const int hl = g & 1;  // non-R8: this lane's column is the lo part when odd
-      const int tok[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
-      const uint32_t* vtile = reinterpret_cast<const uint32_t*>(st + a.st_vc);
-      const char* vm = reinterpret_cast<const char*>(st + a.st_vm);
-      // zero-point sums (per-token values) at the score owners
-      if (vp && VAXIS == 0) {
+      const uint32_t* vtile = reinterpret_cast<const uint32_t*>(st + st_vc);
+      if (VAXIS == 0 && vp) {
 #pragma unroll
-        for (int jg = 0; jg < GV_MAX; ++jg) {
-          if (jg >= (a.V.whole ? 1 : a.V.gpt)) break;
+        for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg) {
+          if (jg < gs_v) {
 #pragma unroll
-          for (int q = 0; q < SL::N; ++q) {
-            const int row = g + 8 * SL::rh(q);
-            float zf, stp;
-            meta_fold(vm, a.V.whole ? row : row * a.V.gpt + jg, a.V, &zf, &stp);
-            Zs[jg][q] += p[q] * zf;
+            for (int q = 0; q < SL::N; ++q) Zs[jg][q] += p[q] * (SL::rh(q) ? cv_row1 : cv_row0)[jg].y;
           }
         }
       }
@@ -509,54 +685,18 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
         for (int q = 0; q < SL::N; ++q) Pg[q] += p[q];
       }
       uint32_t bh0 = 0, bh1 = 0, bl0 = 0, bl1 = 0;
-      auto make_b = [&](int jg, bool fold) {
-        float x[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float v = pv[u];
-          if (fold) {
-            float zf, stp;
-            meta_fold(vm, a.V.whole ? tok[u] : tok[u] * a.V.gpt + jg, a.V, &zf, &stp);
-            v = v * stp * sc_v;
-          }
-          x[u] = v;
-        }
-        __half h[4], l[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) split_hl(x[u], &h[u], &l[u]);
-        bh0 = pack_h2(h[0], h[1]);
-        bh1 = pack_h2(h[2], h[3]);
-        bl0 = pack_h2(l[0], l[1]);
-        bl1 = pack_h2(l[2], l[3]);
+      auto make_b = [&](float x0, float x1, float x2, float x3) {
+        const __half2 h01 = __floats2half2_rn(x0, x1), h23 = __floats2half2_rn(x2, x3);
+        const float2 f01 = __half22float2(h01), f23 = __half22float2(h23);
+        const __half2 l01 = __floats2half2_rn(x0 - f01.x, x1 - f01.y);
+        const __half2 l23 = __floats2half2_rn(x2 - f23.x, x3 - f23.y);
+        bh0 = *reinterpret_cast<const uint32_t*>(&h01);
+        bh1 = *reinterpret_cast<const uint32_t*>(&h23);
+        bl0 = *reinterpret_cast<const uint32_t*>(&l01);
+        bl1 = *reinterpret_cast<const uint32_t*>(&l23);
       };
-      const int cpg_v = (VAXIS == 0) ? (a.V.whole ? NCH : a.V.group / 16) : NCH;
-      if (!vp || VAXIS == 1) make_b(0, false);
-#pragma unroll
-      for (int j = 0; j < NCH; ++j) {
-        if (vp && VAXIS == 0 && (j % cpg_v) == 0) make_b(j / cpg_v, true);
-        uint32_t A[4];
-        if (vp) {
-          switch (a.V.bits) {
-            case 2: convert_chunk<2, D>(vtile, lane, j, A); break;
-            case 3: convert_chunk<3, D>(vtile, lane, j, A); break;
-            case 4: convert_chunk<4, D>(vtile, lane, j, A); break;
-            case 5: convert_chunk<5, D>(vtile, lane, j, A); break;
-            case 6: convert_chunk<6, D>(vtile, lane, j, A); break;
-            case 7: convert_chunk<7, D>(vtile, lane, j, A); break;
-            default: convert_chunk<8, D>(vtile, lane, j, A); break;
-          }
-        } else {
-          // fp16 tail: rows = channels 16j + g (+8), columns = tokens 2tig (+1) (+8)
-          const __half* tb = vtail + (long)(t0 - sealed_v) * D + 16 * j + g;
-          auto pr = [&](int t, int coff) -> uint32_t {
-            return pack_h2(tb[(long)t * D + coff], tb[(long)(t + 1) * D + coff]);
-          };
-          A[0] = pr(2 * tig, 0);
-          A[1] = pr(2 * tig, 8);
-          A[2] = pr(2 * tig + 8, 0);
-          A[3] = pr(2 * tig + 8, 8);
-        }
-        if (vp && VAXIS == 1) {
+      auto mma_v = [&](int j, const uint32_t* A, bool into_group) {
+        if (VAXIS == 1 && into_group) {
           if (!R8) {
             mma_16816(Og[VAXIS == 1 ? j : 0], A[0], A[1], A[2], A[3], hl ? bl0 : bh0, hl ? bl1 : bh1);
           } else {
@@ -571,10 +711,50 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
             mma_16816(O[j], A[0], A[1], A[2], A[3], bl0, bl1);
           }
         }
+      };
+      auto pv_packed = [&](auto vb) {
+        constexpr int VB = decltype(vb)::value;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          if (VAXIS == 0 && (j & (cpgv - 1)) == 0) {
+            const int jg = j >> lg_cpgv;
+            make_b(pv[0] * cv_t0[jg].x, pv[1] * cv_t1[jg].x, pv[2] * cv_t2[jg].x, pv[3] * cv_t3[jg].x);
+          }
+          uint32_t A[4];
+          convert_chunk<VB, D>(vtile, lane, j, A);
+          mma_v(j, A, true);
+        }
+      };
+      if (vp) {
+        if (VAXIS == 1) make_b(pv[0], pv[1], pv[2], pv[3]);
+        switch (vbits) {
+          case 2: pv_packed(IntC<2>{}); break;
+          case 3: pv_packed(IntC<3>{}); break;
+          case 4: pv_packed(IntC<4>{}); break;
+          case 5: pv_packed(IntC<5>{}); break;
+          case 6: pv_packed(IntC<6>{}); break;
+          case 7: pv_packed(IntC<7>{}); break;
+          default: pv_packed(IntC<8>{}); break;
+        }
+      } else {
+        make_b(pv[0], pv[1], pv[2], pv[3]);
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          // fp16 tail: rows = channels 16j + g (+8), columns = tokens 2tig (+1) (+8)
+          const __half* tb = vtail + (long)(t0 - sealed_v) * D + 16 * j + g;
+          auto pr = [&](int t, int coff) -> uint32_t {
+            return pack_h2(tb[(long)t * D + coff], tb[(long)(t + 1) * D + coff]);
+          };
+          uint32_t A[4];
+          A[0] = pr(2 * tig, 0);
+          A[1] = pr(2 * tig, 8);
+          A[2] = pr(2 * tig + 8, 0);
+          A[3] = pr(2 * tig + 8, 8);
+          mma_v(j, A, false);
+        }
       }
-      // per-channel values: flush the group at its last tile
-      if (VAXIS == 1 && vp && ((t0 + kTile) % a.V.group) == 0) {
-        // P sums per query: reduce over the 8 token rows and both row halves
+      // per-channel values: apply the group's steps and zero points at its last tile
+      if (vflush) {
         float ps[SL::N];
 #pragma unroll
         for (int q = 0; q < SL::N; ++q) {
@@ -583,23 +763,15 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
           for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           ps[q] = v;
         }
-        float pc0, pc1;  // query sums for this thread's two O columns
-        if (!R8) {
-          pc0 = ps[0] + ps[1];
-          pc1 = 0.0f;  // lo column carries no zero-point term
-        } else {
-          pc0 = ps[0] + ps[2];
-          pc1 = ps[1] + ps[3];
-        }
+        const float pc0 = R8 ? (ps[0] + ps[2]) : (ps[0] + ps[1]);
+        const float pc1 = R8 ? (ps[1] + ps[3]) : 0.0f;  // non-R8: the lo column carries no zero term
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
-            const int c = 16 * j + g + 8 * rr;
-            float zf, stp;
-            meta_fold(vm, c, a.V, &zf, &stp);
-            O[j][2 * rr + 0] += stp * Og[VAXIS == 1 ? j : 0][2 * rr + 0] + zf * pc0;
-            O[j][2 * rr + 1] += stp * Og[VAXIS == 1 ? j : 0][2 * rr + 1] + zf * pc1;
+            const float2 m = canV[16 * j + g + 8 * rr];
+            O[j][2 * rr + 0] += m.x * Og[VAXIS == 1 ? j : 0][2 * rr + 0] + m.y * pc0;
+            O[j][2 * rr + 1] += m.x * Og[VAXIS == 1 ? j : 0][2 * rr + 1] + m.y * pc1;
             Og[VAXIS == 1 ? j : 0][2 * rr + 0] = 0.0f;
             Og[VAXIS == 1 ? j : 0][2 * rr + 1] = 0.0f;
           }
@@ -610,18 +782,14 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
     }
 
     __syncwarp();
-    if (lane == 0 && i + a.nstages < ntl) {
+    if (lane == 0 && i + ns < ntl) {
       fence_proxy_async();
-      issue(i + a.nstages);
+      issue(i + ns);
     }
   }
-  if (failed) {
+  if (failed && lane == 0) {
     // give copies still in flight a bounded chance to land before the CTA exits
-    if (lane == 0)
-      for (int i = 0; i < min(ntl, a.nstages); ++i) {
-        const int s = i % a.nstages;
-        mbar_wait_bounded(&bars[s], 0u, nullptr);
-      }
+    for (int s = 0; s < min(ntl, ns); ++s) mbar_wait_bounded(&bars[s], 0u, nullptr);
   }
 
   // ---- warp epilogue: complete l and the per-token value zero-point sums
@@ -644,10 +812,9 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
     mq0 = m_run[0];
     mq1 = m_run[1];
   }
-  // per-token values: O (in units of 2^E_v) -> true units, plus zero-point sums
   if (VAXIS == 0) {
 #pragma unroll
-    for (int jg = 0; jg < GV_MAX; ++jg)
+    for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
 #pragma unroll
       for (int q = 0; q < SL::N; ++q) {
         float v = Zs[jg][q];
@@ -657,12 +824,10 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
       }
   }
   __syncthreads();  // stages are free: reuse them for the CTA merge
-  float* mw = reinterpret_cast<float*>(smem + a.head_bytes);  // [4][rep][D+2]
+  float* mw = reinterpret_cast<float*>(smem + CFG::head_bytes(a));  // [4][rep][D+2]
   const int rowlen = D + 2;
-  // write this warp's (m, l, O) per query
   {
-    const int gcnt = (VAXIS == 0) ? (a.V.whole ? 1 : a.V.gpt) : 1;
-    const int gsz = (VAXIS == 0) ? (a.V.whole ? D : a.V.group) : D;
+    const int lg_gsz = (VAXIS == 0 && !vwhole) ? v_lgG : 30;  // channel group of an output column
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
 #pragma unroll
@@ -682,15 +847,14 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
           rho1 = 2 * tig + 1;
         }
         if (VAXIS == 0) {
-          const int jg = c / gsz;
+          const int jg = c >> lg_gsz;
           float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-          for (int u = 0; u < GV_MAX; ++u)
+          for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u)
             if (u == jg) {
               z0 = R8 ? (Zs[u][0] + Zs[u][2]) : (Zs[u][0] + Zs[u][1]);
               z1 = R8 ? (Zs[u][1] + Zs[u][3]) : 0.0f;
             }
-          (void)gcnt;
           v0 = v0 * inv_sc_v + z0;
           v1 = v1 * inv_sc_v + z1;
         }
@@ -714,7 +878,8 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
   }
   __syncthreads();
   // CTA merge -> chunk partial in the workspace
-  const long hqb = (long)b * a.H * rep + hq0;
+  const long hqb = (long)b * H * rep + hq0;
+  const int max_chunks = a.max_chunks;
   for (int i = threadIdx.x; i < rep * rowlen; i += blockDim.x) {
     const int rho = i / rowlen, c = i % rowlen;
     float M = -INFINITY;
@@ -730,14 +895,14 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
         acc += f * mw[(w * rep + rho) * rowlen + c];
       }
     }
-    a.work[((hqb + rho) * a.max_chunks + chunk) * rowlen + c] = acc;
+    a.work[((hqb + rho) * max_chunks + chunk) * rowlen + c] = acc;
   }
   // the last CTA of (b, h) combines all chunks
   __shared__ int last;
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned prev = atomicAdd(a.tickets + bh, 1u);
+    const unsigned prev = atomicAdd(a.tickets + bh, 1u);
     last = (prev == (unsigned)nchunks - 1u);
   }
   __syncthreads();
@@ -745,7 +910,7 @@ __global__ void __launch_bounds__(128) decode_kernel(DecodeArgs a) {
   __threadfence();
   for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
     const int rho = i / D, c = i % D;
-    const float* pbase = a.work + (hqb + rho) * a.max_chunks * (long)rowlen;
+    const float* pbase = a.work + (hqb + rho) * max_chunks * (long)rowlen;
     float M = -INFINITY;
     for (int k = 0; k < nchunks; ++k) M = fmaxf(M, __ldcg(pbase + (long)k * rowlen + D));
     float num = 0.0f, den = 0.0f;

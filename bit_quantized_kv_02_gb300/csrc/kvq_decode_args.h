@@ -5,13 +5,26 @@
 
 namespace kvq {
 
-// ------------------------------------------------------------ arguments ----
+// One tensor (keys or values) of the decoded layer, resolved on the host so
+// the kernel's hot loop only does shifts, masks and adds.
+struct DecTensor {
+  const char* codes;    // packed tiles of the layer: [B][H][ntiles][tile_bytes]
+  const char* meta;     // metadata of the layer
+  const __half* tail;   // fp16 tail of the layer (per-channel axis): [B][H][G][D]
+  int bits, sym, meta_f32, axis, whole;
+  int lg_group;         // log2 of the group size (tokens per-channel, channels per-token); 0 when whole
+  int group;            // group size (per-channel: tokens)
+  int gpt;              // per-token axis: groups per head row (1 when whole)
+  int meta_bytes;       // bytes of one stored entry
+  int tile_bytes;       // packed bytes of one 16-token tile
+  int mtile_bytes;      // per-token: metadata bytes per tile; per-channel: per group
+};
 
 struct DecodeArgs {
-  TensorLayout K, V;
-  int layer, B, H, rep, tcap, ntiles;
-  const char* base;
+  DecTensor K, V;
+  int B, H, rep, tcap, ntiles;
   const int32_t* lens;      // [B] of this layer
+  const uint32_t* smax_k;   // [B][H] largest key step of this layer (float bits)
   const uint32_t* smax_v;   // [B][H] largest value step of this layer (float bits)
   const void* q;
   int q_f32;
@@ -23,20 +36,57 @@ struct DecodeArgs {
   float* out;               // [B][H*rep][D]
   int* err;
   // shared-memory plan (bytes)
-  int nstages, stage_bytes;
+  int lg_nstages, stage_bytes;
   int st_kc, st_km, st_vc, st_vm;  // offsets inside a stage
-  int kc_bytes, vc_bytes;          // packed tile bytes
-  int km_tile_bytes, vm_tile_bytes;  // per-token metadata bytes per tile
-  int km_group_bytes, vm_group_bytes;  // per-channel metadata bytes per group
-  int warp_bytes;           // per-warp region: B operand area + stages + barriers
+  int warp_bytes;           // per-warp region: B operand + canonical metadata + stages + barriers
   int barea_bytes;
+  int canon_k, canon_v;     // canonical (step, zero') entries per warp for keys / values
+  int stage_off;            // offset of the stage ring inside the per-warp region
   int head_bytes;           // CTA head region (q, group sums)
 };
 
+// Shared-memory plan of the decode kernel; one constexpr function serves the
+// host planner and the compile-time specialisations, so both always agree.
+struct DecLayout {
+  int kc_bytes, vc_bytes, km_bytes, vm_bytes;  // packed tile / metadata bytes per stage
+  int st_kc, st_km, st_vc, st_vm;              // offsets inside a stage
+  int stage_bytes, lg_ns;                      // stage size, log2 of the stage count
+  int barea_bytes, canon_k, canon_v, stage_off, warp_bytes, head_bytes;
+};
+
+__host__ __device__ constexpr int dl_round(int x, int m) { return (x + m - 1) / m * m; }
+__host__ __device__ constexpr int dl_max(int x, int y) { return x > y ? x : y; }
+
+__host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, int kaxis, int kwhole, int kgpt,
+                                                   int kmb, int vbits, int vaxis, int vwhole, int vgpt, int vmb) {
+  DecLayout L{};
+  L.kc_bytes = D * kbits * 2;
+  L.vc_bytes = D * vbits * 2;
+  L.km_bytes = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) * kmb : D * kmb;
+  L.vm_bytes = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) * vmb : D * vmb;
+  L.st_kc = 0;
+  L.st_km = dl_round(L.st_kc + L.kc_bytes, 16);
+  L.st_vc = dl_round(L.st_km + L.km_bytes, 16);
+  L.st_vm = dl_round(L.st_vc + L.vc_bytes, 16);
+  L.stage_bytes = dl_round(L.st_vm + L.vm_bytes, 128);
+  L.lg_ns = L.stage_bytes <= 4096 ? 2 : 1;
+  L.barea_bytes = (D / 16) * 32 * 8 * (rep == 8 ? 2 : 1);
+  L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : D;
+  L.canon_v = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) : D;
+  L.stage_off = dl_round(L.barea_bytes + (L.canon_k + L.canon_v) * 8 + 32, 128);
+  L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns) + (8 << L.lg_ns), 128);
+  const int merge_bytes = 4 * rep * (D + 2) * 4;
+  if (L.warp_bytes * 4 < merge_bytes) L.warp_bytes = dl_round((merge_bytes + 3) / 4, 128);
+  L.head_bytes = dl_round((rep * D + (kaxis == 0 ? kgpt * rep : 0)) * 4, 128);
+  return L;
+}
 
 // per-head-dim kernel entry points (one translation unit each, compiled in parallel)
 void* decode_kernel_ptr_d64(bool r8, int vaxis);
 void* decode_kernel_ptr_d128(bool r8, int vaxis);
 void* decode_kernel_ptr_d256(bool r8, int vaxis);
+
+// compile-time specialisation for this cache's formats, or null (generic kernel)
+void* decode_kernel_fast(const kvq_cache* C);
 
 }  // namespace kvq

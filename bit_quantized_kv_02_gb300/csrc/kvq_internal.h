@@ -28,6 +28,8 @@ struct kvq_cache {
   int plan_tokens = 0;  // decode split plan assumes at least this many tokens per sequence
   size_t dec_smem = 0;  // dynamic shared memory of the decode kernel
   int dec_occ = 1;      // resident decode CTAs per SM
+  void* dec_fn = nullptr;  // decode kernel in use (compile-time specialisation or generic)
+  int generic_decode = 0;  // 1: always use the generic (runtime-format) decode kernel
 };
 
 namespace kvq {
@@ -54,6 +56,7 @@ size_t append_smem(const kvq_cache* C);
 // one-time kernel attribute set-up at cache creation (keeps launches capturable)
 cudaError_t quant_setup(kvq_cache* C);
 cudaError_t decode_setup(kvq_cache* C);
+void* decode_kernel_fast(const kvq_cache* C);
 
 // decode: plans the split, launches the split-K kernel (which also combines)
 cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,

@@ -283,108 +283,126 @@ struct AppendArgs {
   QuantArgs k, v;       // x points at [B][H][D] new tokens (t_stride unused)
   int32_t* lens;        // device lens of the layer
   uint32_t* tickets;    // [B]
+  int warp_smem;        // per-warp scratch bytes for the per-token path
 };
 
-// Append the new token of (b, h) to one tensor.  `n` = old length.
-__device__ void append_tensor(const QuantArgs& a, int b, int h, int n, unsigned char* smem) {
+// One warp appends the new token of (b, h) (old length n) to one tensor: a
+// per-token tensor quantizes the token row now and merges its codes into the
+// tile words that hold that row; a per-channel tensor stores it in the fp16
+// tail and reports (returns true) when the tail just filled up, so that the
+// caller seals the group with the whole CTA.  xs / cs: per-warp shared scratch.
+__device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, uint8_t* cs, float* zs, float* ss) {
+  const int lane = threadIdx.x & 31;
   const int D = a.D;
   const long xs_t = (long)a.H * D;
-  const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
-  if (a.L.axis == 1) {  // per channel: tail, seal when full
+  if (a.L.axis == 1) {
     const int G = a.L.group;
-    const int slot = n % G;
+    const int slot = n & (G - 1);
     __half* tail = tail_ptr(a, b, h);
-    for (int c = threadIdx.x; c < D; c += blockDim.x)
+    for (int c = lane; c < D; c += 32)
       tail[(long)slot * D + c] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
-    if (slot != G - 1) return;
-    __syncthreads();  // the block's own tail writes are visible to the block
-    float* xs = reinterpret_cast<float*>(smem);
-    uint8_t* cs = reinterpret_cast<uint8_t*>(xs + G * D);
-    float* zs = reinterpret_cast<float*>(cs + G * D);
-    float* ss = zs + D;
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) xs[i] = __half2float(tail[i]);
-    __syncthreads();
-    quant_channel_block(a, b, h, n / G, xs, cs, zs, ss);
-    __syncthreads();
-    return;
+    return slot == G - 1;
   }
-  // per token: quantize the token row now and merge it into its tile
   const int whole = a.L.whole;
   const int nh = whole ? a.H : 1;
   const int rowlen = nh * D;
   const int G = whole ? rowlen : a.L.group;
   const int gpr = rowlen / G;
-  float* xs = reinterpret_cast<float*>(smem);                  // [rowlen]
-  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + rowlen);       // [nh][16][D] (row trow only)
-  float* zs = reinterpret_cast<float*>(cs + kTile * rowlen);   // [gpr]
-  float* ss = zs + gpr;
-  for (int i = threadIdx.x; i < rowlen; i += blockDim.x) xs[i] = load_in(a.x, (long)b * xs_t + (long)h * D + i, a.x_f32);
-  __syncthreads();
+  for (int c = lane; c < rowlen; c += 32) xs[c] = load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32);
+  __syncwarp();
   char* meta = meta_ptr(a);
   float smax_local = 0.0f;
-  for (int j = warp; j < gpr; j += nwarp) {
+  for (int j = 0; j < gpr; ++j) {
     float mn, mx, am;
     warp_stats(xs + j * G, G, 1, &mn, &mx, &am);
     float z, s;
     group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
-    if ((threadIdx.x & 31) == 0) {
+    smax_local = fmaxf(smax_local, s);
+    if (lane == 0) {
       zs[j] = z;
       ss[j] = s;
-      long mi = whole ? ((long)b * a.tcap + n) : ((((long)b * a.H + h) * a.tcap + n) * gpr + j);
+      const long mi = whole ? ((long)b * a.tcap + n) : ((((long)b * a.H + h) * a.tcap + n) * gpr + j);
       store_meta(meta, mi, a.L.meta_f32, a.L.sym, z, s);
-      smax_local = fmaxf(smax_local, s);
     }
   }
-  __syncthreads();
-  const int trow = n % kTile, tile = n / kTile;
-  for (int i = threadIdx.x; i < rowlen; i += blockDim.x) {
-    int hh = i / D, c = i % D;
-    cs[(hh * kTile + trow) * D + c] = (uint8_t)quant_code(xs[i], zs[i / G], ss[i / G], a.L.bits, a.L.sym);
-  }
-  __syncthreads();
+  __syncwarp();
+  for (int c = lane; c < rowlen; c += 32) cs[c] = (uint8_t)quant_code(xs[c], zs[c / G], ss[c / G], a.L.bits, a.L.sym);
+  __syncwarp();
+  // merge into the tile words that hold token row trow
+  const int trow = n & 15, tile = n >> 4;
+  const Planes& pl = a.L.planes;
   for (int hh = 0; hh < nh; ++hh) {
     uint32_t* dst = codes_ptr(a, b, h + hh, tile);
-    const uint8_t* tc = cs + hh * kTile * D;
-    for (int wi = threadIdx.x; wi < a.L.tile_words; wi += blockDim.x) {
-      uint32_t m = word_token_mask(D, a.L.planes, a.is_value, wi, trow);
-      if (!m) continue;
-      // build_word reads only row trow where m is set; other rows contribute garbage masked off below
-      uint32_t nv = 0;
-      {
-        int p = 0;
-        for (int q = 1; q < a.L.planes.n; ++q)
-          if (wi >= D * a.L.planes.off[q] / 2) p = q;
-        int w = a.L.planes.w[p];
-        int W = D * w / 64, P = 16 / w;
-        int rel = wi - D * a.L.planes.off[p] / 2;
-        int lane = rel / W, ii = rel % W;
-        uint32_t mk = (1u << w) - 1u;
+    const uint8_t* tc = cs + hh * D;
+    for (int p = 0; p < pl.n; ++p) {
+      const int w = pl.w[p], off = pl.off[p];
+      const int W = D * w / 64, P = 16 / w;
+      const uint32_t mk = (1u << w) - 1u;
+      // keys: the 4 lanes of fragment row trow; values: the 8 lanes of fragment column trow
+      const int nl = a.is_value ? 8 : 4;
+      for (int idx = lane; idx < nl * W; idx += 32) {
+        const int li = idx / W, i = idx % W;
+        const int ln = a.is_value ? (4 * li + ((trow & 7) >> 1)) : (4 * (trow & 7) + li);
+        uint32_t m = 0, nv = 0;
         for (int k = 0; k < P; ++k)
           for (int e = 0; e < 2; ++e) {
             int t, c;
-            elem_of(a.is_value, lane, ii * P + k, e, &t, &c);
-            if (t == trow) nv |= (((uint32_t)tc[t * D + c] >> a.L.planes.off[p]) & mk) << (k * w + 16 * e);
+            elem_of(a.is_value, ln, i * P + k, e, &t, &c);
+            if (t == trow) {
+              m |= mk << (k * w + 16 * e);
+              nv |= (((uint32_t)tc[c] >> off) & mk) << (k * w + 16 * e);
+            }
           }
+        if (!m) continue;
+        const int wi = D * off / 2 + ln * W + i;
+        const uint32_t old = trow == 0 ? 0u : dst[wi];  // a fresh tile starts from zero bits
+        dst[wi] = (old & ~m) | nv;
       }
-      uint32_t old = (trow == 0) ? 0u : dst[wi];  // a fresh tile starts from zero bits
-      dst[wi] = (old & ~m) | nv;
     }
   }
-  if ((threadIdx.x & 31) == 0 && smax_local > 0.0f)
+  if (lane == 0 && smax_local > 0.0f)
     for (int hh = 0; hh < nh; ++hh) atomic_max_pos(a.smax + (long)b * a.H + h + hh, smax_local);
-  __syncthreads();
+  return false;
 }
 
-// One CTA per (sequence, kv head): append K then V; the last CTA of a
-// sequence advances its length (atomic ticket, no waiting).
-__global__ void append_kernel(AppendArgs a) {
+// One CTA of 128 threads per (sequence, kv head): warp 0 appends the key, warp 1
+// the value; a per-channel tensor whose tail just filled up is then sealed by
+// all four warps.  The last CTA of a sequence advances its length (atomic
+// ticket, no waiting).
+__global__ void append_kernel(const __grid_constant__ AppendArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int seal[2];
   const int b = blockIdx.x, h = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
   const int n = a.lens[b];
-  if (!(a.k.L.whole && h != 0)) append_tensor(a.k, b, h, n, smem);
+  const QuantArgs& t = warp == 0 ? a.k : a.v;
+  if (threadIdx.x < 2) seal[threadIdx.x] = 0;
   __syncthreads();
-  if (!(a.v.L.whole && h != 0)) append_tensor(a.v, b, h, n, smem);
+  if (warp < 2 && !(t.L.whole && h != 0)) {
+    const int rowlen = (t.L.whole ? t.H : 1) * t.D;
+    unsigned char* base = smem + warp * a.warp_smem;
+    float* xs = reinterpret_cast<float*>(base);
+    float* zs = xs + rowlen;
+    float* ss = zs + 16;
+    uint8_t* cs = reinterpret_cast<uint8_t*>(ss + 16);
+    const bool full = append_warp(t, b, h, n, xs, cs, zs, ss);
+    if (full && (threadIdx.x & 31) == 0) seal[warp] = 1;
+  }
   __syncthreads();
+  for (int w = 0; w < 2; ++w) {
+    if (!seal[w]) continue;
+    const QuantArgs& q = w == 0 ? a.k : a.v;
+    const int G = q.L.group, D = q.D;
+    float* xs = reinterpret_cast<float*>(smem);
+    uint8_t* cs = reinterpret_cast<uint8_t*>(xs + G * D);
+    float* zs = reinterpret_cast<float*>(cs + G * D);
+    float* ss = zs + D;
+    const __half* tail = tail_ptr(q, b, h);
+    for (int i = threadIdx.x; i < G * D; i += blockDim.x) xs[i] = __half2float(tail[i]);
+    __syncthreads();
+    quant_channel_block(q, b, h, n / G, xs, cs, zs, ss);
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
     __threadfence();
     unsigned prev = atomicAdd(a.tickets + b, 1u);
@@ -526,20 +544,22 @@ cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v
   return cudaGetLastError();
 }
 
-size_t append_smem(const kvq_cache* C) {
+static int append_warp_smem(const kvq_cache* C) {
   const int H = C->cfg.kv_heads, D = C->cfg.head_dim;
-  size_t m = 0;
+  int m = 0;
   const TensorLayout* ls[2] = {&C->k, &C->v};
   for (int i = 0; i < 2; ++i) {
-    const TensorLayout& L = *ls[i];
-    size_t s;
-    if (L.axis == 1) s = channel_smem(L.group, D);
-    else {
-      int rowlen = (L.whole ? H : 1) * D;
-      s = (size_t)rowlen * 4 + (size_t)kTile * rowlen + (size_t)rowlen * 8 + 16;
-    }
-    m = s > m ? s : m;
+    const int rowlen = (ls[i]->whole ? H : 1) * D;
+    m = std::max(m, rowlen * 5 + 128 + 16);
   }
+  return (m + 15) / 16 * 16;
+}
+
+size_t append_smem(const kvq_cache* C) {
+  size_t m = 2 * (size_t)append_warp_smem(C);
+  const TensorLayout* ls[2] = {&C->k, &C->v};
+  for (int i = 0; i < 2; ++i)
+    if (ls[i]->axis == 1) m = std::max(m, channel_smem(ls[i]->group, C->cfg.head_dim));
   return m;
 }
 
@@ -550,8 +570,9 @@ cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v,
   a.v = make_args(C, 1, layer, v, x_f32, 1);
   a.lens = C->d_lens + (long)layer * C->cfg.batch;
   a.tickets = C->d_append_tickets;
+  a.warp_smem = append_warp_smem(C);
   size_t sm = append_smem(C);
-  append_kernel<<<dim3(C->cfg.batch, C->cfg.kv_heads), 256, sm, st>>>(a);
+  append_kernel<<<dim3(C->cfg.batch, C->cfg.kv_heads), 128, sm, st>>>(a);
   ++*launches;
   return cudaGetLastError();
 }

@@ -56,7 +56,8 @@ _lib = None
 EXPORTED = ["kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_prefill_quantize", "kvq_append",
             "kvq_decode_attn", "kvq_export", "kvq_cache_tcap", "kvq_get_lens", "kvq_decode_traffic",
             "kvq_device_status", "kvq_last_launches", "kvq_status_string", "kvq_last_error",
-            "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static"]
+            "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static", "kvq_set_decode_kernel",
+            "kvq_decode_kernel_specialized"]
 
 
 def lib():
@@ -87,12 +88,16 @@ def lib():
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_decode_attn_static.argtypes = [P, I, P, I, ctypes.c_float, P, P]
         L.kvq_set_decode_plan.argtypes = [P, I]
+        L.kvq_set_decode_kernel.argtypes = [P, I]
+        L.kvq_decode_kernel_specialized.argtypes = [P]
+        L.kvq_decode_kernel_specialized.restype = I
         L.kvq_refresh_lens.argtypes = [P, P]
         L.kvq_last_error.argtypes = [P]
         L.kvq_last_error.restype = ctypes.c_char_p
         for name in ("kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_prefill_quantize",
                      "kvq_append", "kvq_decode_attn", "kvq_export", "kvq_get_lens", "kvq_decode_traffic",
-                     "kvq_device_status", "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static"):
+                     "kvq_device_status", "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static",
+                     "kvq_set_decode_kernel"):
             getattr(L, name).restype = S
         _lib = L
         return L
@@ -249,6 +254,13 @@ class KVQCache:
 
     def kvq_set_decode_plan(self, plan_tokens: int):
         _check(lib().kvq_set_decode_plan(self.handle, int(plan_tokens)), "kvq_set_decode_plan")
+
+    def kvq_set_decode_kernel(self, which: int):
+        """0: compile-time specialisation when one matches (default); 1: generic kernel."""
+        _check(lib().kvq_set_decode_kernel(self.handle, int(which)), "kvq_set_decode_kernel", self.handle)
+
+    def kvq_decode_kernel_specialized(self) -> bool:
+        return bool(lib().kvq_decode_kernel_specialized(self.handle))
 
     def kvq_refresh_lens(self, stream=None):
         _check(lib().kvq_refresh_lens(self.handle, _stream(stream)), "kvq_refresh_lens", self.handle)

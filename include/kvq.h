@@ -209,6 +209,16 @@ kvq_status kvq_device_status(kvq_cache_t cache, void* stream);
  * step needs.  0 (default) plans for the current lengths. */
 kvq_status kvq_set_decode_plan(kvq_cache_t cache, int plan_tokens);
 
+/* Decode kernel choice: which = 0 (default) uses a compile-time specialisation
+ * of the decode kernel when the cache's formats match one (fp16 metadata, no
+ * whole-vector groups, formats of the benchmarked workloads), else the generic
+ * kernel; which = 1 always uses the generic (runtime-format) kernel.  Both
+ * compute the same result; the choice only affects speed. */
+kvq_status kvq_set_decode_kernel(kvq_cache_t cache, int which);
+
+/* 1 if kvq_decode_attn currently runs a compile-time specialisation, else 0. */
+int kvq_decode_kernel_specialized(kvq_cache_t cache);
+
 /* Replayed graphs advance the device lengths only; this copies them back into
  * the host mirror (synchronises `stream`). */
 kvq_status kvq_refresh_lens(kvq_cache_t cache, void* stream);

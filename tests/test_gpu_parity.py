@@ -59,10 +59,17 @@ def decode_ref(wl, orq_k, orq_v, lens, q_cpu, scale):
     return oracle.attention(kh, vh, q_cpu.float().numpy(), np.array(lens, np.int32), scale)
 
 
-def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0):
-    """Prefill `lens` tokens of layer `layer`, compare the export and the decode output."""
+def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0, generic=None):
+    """Prefill `lens` tokens of layer `layer`, compare the export and the decode output.
+    generic: None keeps the default kernel choice, True forces the generic kernel,
+    False requires the compile-time specialisation."""
     T = max(max(lens), 1)
     cache = make_cache(wl, max_tokens=T, max_splits=max_splits, meta_dtype=kvq.F32 if meta_f32 else kvq.F16)
+    if generic is True:
+        cache.kvq_set_decode_kernel(1)
+        assert not cache.kvq_decode_kernel_specialized()
+    elif generic is False:
+        assert cache.kvq_decode_kernel_specialized()
     k, v = wl.layer_kv(layer, "cpu", T=T)
     lens_l = [int(x) for x in lens]
     cache.kvq_prefill_quantize(layer, k.cuda(), v.cuda(), lens_l)
@@ -127,6 +134,26 @@ def test_parity_cases(case):
     name, B, Hq, H, D, kc, vc, lens = case
     wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=3)
     run_case(wl, lens)
+
+
+# formats that have a compile-time specialisation of the decode kernel
+FAST_CASES = [
+    ("fast_d64_k4pc_v4pt", 2, 2, 2, 64, (4, 32, PC, ASYM), (4, 32, PT, ASYM), [700, 65]),
+    ("fast_d64_k6v4_pt64", 2, 2, 2, 64, (6, 64, PT, ASYM), (4, 64, PT, ASYM), [300, 17]),
+    ("fast_d128_k2pc_v2pt", 2, 2, 2, 128, (2, 32, PC, ASYM), (2, 32, PT, ASYM), [4113, 100]),
+    ("fast_d128_gqa4", 2, 8, 2, 128, (2, 64, PC, ASYM), (2, 64, PT, ASYM), [1500, 64]),
+    ("fast_d256_gqa8_pt", 1, 8, 1, 256, (4, 32, PT, ASYM), (8, 32, PT, ASYM), [1000]),
+    ("fast_d256_gqa8_pc", 1, 8, 1, 256, (4, 32, PC, ASYM), (8, 32, PT, ASYM), [777]),
+    ("fast_d256_sym6", 1, 16, 2, 256, (6, 32, PT, SYM), (6, 32, PT, SYM), [600]),
+]
+
+
+@pytest.mark.parametrize("generic", [False, True], ids=["specialized", "generic"])
+@pytest.mark.parametrize("case", FAST_CASES, ids=[c[0] for c in FAST_CASES])
+def test_specialized_and_generic_kernels(case, generic):
+    name, B, Hq, H, D, kc, vc, lens = case
+    wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=7)
+    run_case(wl, lens, generic=generic)
 
 
 @pytest.mark.parametrize("case", CASES[:6] + CASES[12:], ids=[c[0] for c in CASES[:6] + CASES[12:]])
