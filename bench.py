@@ -47,7 +47,15 @@ L2_FLUSH_BYTES = 256 << 20
 DECODE_SOURCES = ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_args.h", "kvq_common.cuh"]
 
 
-def workload(name: str, batch_scale=1) -> synth.Workload:
+def workload(name: str, tokens: int = 0) -> synth.Workload:
+    wl = _workload(name)
+    if tokens:
+        wl.lens = [min(int(x), tokens) for x in wl.lens]
+        wl.name += f"_t{tokens}"
+    return wl
+
+
+def _workload(name: str) -> synth.Workload:
     if name == "gpt2_small":
         return synth.gpt2_small(kbits=4, vbits=4, kgroup=32, vgroup=32, kaxis=synth.PC, vaxis=synth.PT)
     if name == "gpt2_small_k6v4":
@@ -149,7 +157,7 @@ def make_event(external: bool):
 def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    wl = workload(args.workload)
+    wl = workload(args.workload, args.tokens)
     # weak scaling: each rank owns `batch` sequences of its own (its shard of the job)
     B = wl.batch
     L = wl.layers
@@ -342,6 +350,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="gpt2_small")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--tokens", type=int, default=0, help="cap the cached tokens per sequence (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -350,7 +359,7 @@ def main():
         # the reference arm is the CPU oracle; under torchrun only rank 0 works
         if rank != 0:
             return
-        wl = workload(args.workload)
+        wl = workload(args.workload, args.tokens)
         import oracle
         oracle.build()
         gbs, desc, per = cpu_oracle_sample(wl, seconds=max(1.0, min(20.0, args.cpu_seconds * 0.5 *

@@ -35,7 +35,7 @@ bool valid_tensor(const kvq_tensor_cfg& t, int D, int H) {
 kvq_status validate(const kvq_config* c) {
   if (!c) return KVQ_ERR_INVALID_ARG;
   if (c->layers < 1 || c->batch < 1 || c->kv_heads < 1 || c->q_heads < 1 || c->max_tokens < 1 ||
-      c->max_splits < 0)
+      c->max_splits < 0 || c->max_splits > kMaxSplits)
     return KVQ_ERR_INVALID_ARG;
   if (c->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
   if (c->q_heads % c->kv_heads) return KVQ_ERR_INVALID_ARG;
@@ -83,9 +83,14 @@ int tcap_of(const kvq_config& c) {
   return (c.max_tokens + unit - 1) / unit * unit;
 }
 
+// Default split-K capacity per sequence: enough partitions that a batch fills
+// several waves of a GB300 (152 SMs x ~8 resident CTAs) even when it holds few
+// (sequence, kv head) pairs, never finer than 64 tokens per partition.
 int max_chunks_of(const kvq_config& c, int tcap) {
   if (c.max_splits > 0) return c.max_splits;
-  return std::max(1, (tcap + 511) / 512);
+  const long want = (4L * 152 * 8 + (long)c.batch * c.kv_heads - 1) / ((long)c.batch * c.kv_heads);
+  const long cap = std::max(1, (tcap + 63) / 64);
+  return (int)std::max(1L, std::min(std::min(std::max(want, 8L), cap), (long)kMaxSplits));
 }
 
 // carve the buffer: returns the total size; fills offsets when C != null
@@ -119,13 +124,13 @@ size_t carve(const kvq_config& c, kvq_cache* C) {
   off += align256((size_t)2 * L * B * H * 4);
   size_t at_off = off;
   off += align256((size_t)B * 4);
+  const int mc = max_chunks_of(c, tcap);
   size_t dt_off = off;
-  off += align256((size_t)B * H * 4);
+  off += align256(decode_ticket_words(B, H, mc) * 4);
   size_t err_off = off;
   off += 256;
-  const int mc = max_chunks_of(c, tcap);
   size_t work_off = off;
-  off += align256((size_t)B * c.q_heads * mc * (D + 2) * 4);
+  off += align256(decode_work_floats(B, c.q_heads, (int)D, mc) * 4);
   if (C) {
     C->k = K;
     C->v = V;
@@ -196,7 +201,7 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, const int32_t* lens_host, kvq_
   out->packed = (pk + pv) * cfg->layers;
   out->metadata = (mk + mv) * cfg->layers;
   out->tail = (tk + tv) * cfg->layers;
-  out->workspace = (double)cfg->batch * cfg->q_heads * max_chunks_of(*cfg, tcap) * (cfg->head_dim + 2) * 4.0;
+  out->workspace = (double)decode_work_floats(cfg->batch, cfg->q_heads, cfg->head_dim, max_chunks_of(*cfg, tcap)) * 4.0;
   out->total = out->packed + out->metadata + out->tail + out->workspace;
   double tokens = 0;
   for (int b = 0; b < cfg->batch; ++b) tokens += lens[b];

@@ -30,6 +30,19 @@ namespace kvq {
 constexpr int kTile = 16;         // tokens per packed tile
 constexpr int kWarps = 4;         // warps per decode CTA
 constexpr int kMaxBatch = 1024;   // sequences per cache
+constexpr int kCombineGroup = 16; // split-K partials merged per combine step
+// At most kMaxSplits / kCombineGroup = 64 group partials, so the combine's
+// weights (rep * 66 floats) always fit the CTA merge area (rep * 4 * (D + 2)).
+constexpr int kMaxSplits = 1024;
+
+// split-K workspace: chunk partials + group partials, and combine tickets
+inline int combine_groups(int max_chunks) { return (max_chunks + kCombineGroup - 1) / kCombineGroup; }
+inline size_t decode_work_floats(long batch, long q_heads, int head_dim, int max_chunks) {
+  return (size_t)batch * q_heads * (max_chunks + combine_groups(max_chunks)) * (head_dim + 2);
+}
+inline size_t decode_ticket_words(long batch, long kv_heads, int max_chunks) {
+  return (size_t)batch * kv_heads * (1 + combine_groups(max_chunks));
+}
 
 struct Planes {
   int n;

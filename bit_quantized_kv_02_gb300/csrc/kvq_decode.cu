@@ -65,6 +65,8 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   a.smax_v = C->d_smax + ((long)1 * cfg.layers + layer) * cfg.batch * cfg.kv_heads;
   a.max_chunks = C->max_chunks;
   a.work = C->d_work;
+  a.max_groups = combine_groups(C->max_chunks);
+  a.gwork = C->d_work + (size_t)cfg.batch * cfg.q_heads * C->max_chunks * (D + 2);
   a.tickets = C->d_decode_tickets;
   a.err = C->d_err;
   const DecLayout L = dec_layout(D, rep, C->k.bits, C->k.axis, C->k.whole, C->k.gpt, C->k.meta_bytes, C->v.bits,
@@ -183,6 +185,7 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   if (e != cudaSuccess) return e;
   DecodeArgs& a = P.a;
   a.work = work;
+  a.gwork = work + (size_t)C->cfg.batch * C->cfg.q_heads * C->max_chunks * (C->cfg.head_dim + 2);
   a.tickets = tickets;
   const kvq_config& cfg = C->cfg;
   int unit = kTile;

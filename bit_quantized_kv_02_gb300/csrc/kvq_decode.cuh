@@ -160,11 +160,22 @@ struct IntC {
   static constexpr int value = V;
 };
 
+// stage index of tile i: a constant inside an unrolled block, or i mod stages
+template <int S>
+struct StageC {
+  __device__ static constexpr int get(int) { return S; }
+};
+struct StageR {
+  int mask;
+  __device__ int get(int i) const { return i & mask; }
+};
+
 // ------------------------------------------------------ configurations ---
 
 // Runtime configuration: every format field comes from the launch arguments
 // (the generic kernel, any format the C ABI accepts).
 struct DynCfg {
+  static constexpr int kStaticStages = 0;  // stage count known only at run time
   __device__ static int rep(const DecodeArgs& a) { return a.rep; }
   __device__ static int kbits(const DecodeArgs& a) { return a.K.bits; }
   __device__ static int ksym(const DecodeArgs& a) { return a.K.sym; }
@@ -211,6 +222,7 @@ struct StatCfg {
   static constexpr int KGPT = KAX == 0 ? D / KG : 0, VGPT = VAX == 0 ? D / VG : 0;
   static constexpr int KMB = KSYM ? 2 : 4, VMB = VSYM ? 2 : 4;
   static constexpr DecLayout L = dec_layout(D, REP, KB, KAX, 0, KGPT, KMB, VB, VAX, 0, VGPT, VMB);
+  static constexpr int kStaticStages = 1 << L.lg_ns;
   __device__ static constexpr int rep(const DecodeArgs&) { return REP; }
   __device__ static constexpr int kbits(const DecodeArgs&) { return KB; }
   __device__ static constexpr int ksym(const DecodeArgs&) { return KSYM; }
@@ -451,15 +463,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   const float2* cv_t3 = canV + (tk0 + 9) * gs_v;
   bool failed = false;
 
-  for (int i = 0; i < ntl; ++i) {
-    const int s = i & (ns - 1);
+  // One 16-token tile.  FAST: the tile is full and both its keys and values are
+  // packed (the bulk of every range), so the tail and partial-tile checks fold away.
+  auto tile_body = [&](const int i, auto stag, auto ftag) -> bool {
+    constexpr bool FAST = decltype(ftag)::value != 0;
+    const int s = stag.get(i);
     const int t0 = w0 + i * kTile;
-    if (!mbar_wait_bounded(&bars[s], (uint32_t)((i >> lg_ns) & 1), a.err)) {
-      failed = true;
-      break;
-    }
+    if (!mbar_wait_bounded(&bars[s], (uint32_t)((i >> lg_ns) & 1), a.err)) return false;
     const unsigned char* st = stages + s * stage_bytes;
-    const bool kp = t0 < sealed_k, vp = t0 < sealed_v;
+    const bool kp = FAST || t0 < sealed_k, vp = FAST || t0 < sealed_v;
     const bool vflush = VAXIS == 1 && vp && ((t0 + kTile) & vgmask) == 0;
 
     // ---- metadata of this stage -> canonical fp32 pairs
@@ -576,7 +588,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
     float p[SL::N];
     float alpha[SL::N];
     {
-      if (t0 + kTile > w1) {  // partial last tile of the range
+      if (!FAST && t0 + kTile > w1) {  // partial last tile of the range
 #pragma unroll
         for (int q = 0; q < SL::N; ++q)
           if (t0 + g + 8 * SL::rh(q) >= w1) score[q] = -INFINITY;
@@ -786,6 +798,26 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
       fence_proxy_async();
       issue(i + ns);
     }
+    return true;
+  };
+
+  {
+    // fully packed, full tiles first (unrolled by the stage count when it is a
+    // compile-time constant), then the tail / partial tiles
+    const int lim = min(min(sealed_k, sealed_v), w1);
+    const int nfast = lim > w0 ? (lim - w0) >> 4 : 0;
+    int i = 0;
+    constexpr int NSC = CFG::kStaticStages;
+    if constexpr (NSC == 4) {
+      for (; i + 4 <= nfast && !failed; i += 4)
+        failed = !(tile_body(i, StageC<0>{}, IntC<1>{}) && tile_body(i + 1, StageC<1>{}, IntC<1>{}) &&
+                   tile_body(i + 2, StageC<2>{}, IntC<1>{}) && tile_body(i + 3, StageC<3>{}, IntC<1>{}));
+    } else if constexpr (NSC == 2) {
+      for (; i + 2 <= nfast && !failed; i += 2)
+        failed = !(tile_body(i, StageC<0>{}, IntC<1>{}) && tile_body(i + 1, StageC<1>{}, IntC<1>{}));
+    }
+    for (; i < nfast && !failed; ++i) failed = !tile_body(i, StageR{ns - 1}, IntC<1>{});
+    for (; i < ntl && !failed; ++i) failed = !tile_body(i, StageR{ns - 1}, IntC<0>{});
   }
   if (failed && lane == 0) {
     // give copies still in flight a bounded chance to land before the CTA exits
@@ -897,32 +929,90 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
     }
     a.work[((hqb + rho) * max_chunks + chunk) * rowlen + c] = acc;
   }
-  // the last CTA of (b, h) combines all chunks
+  // Two-level combine behind atomic tickets (no CTA ever waits): the last CTA
+  // of each group of up to kCombineGroup chunks merges the group's partials;
+  // with one group it writes the output, otherwise the group result goes to
+  // the group workspace and the last group merges those.
   __shared__ int last;
+  uint32_t* tk = a.tickets + bh * (1 + a.max_groups);
+  const int grp = chunk / kCombineGroup;
+  const int ngroups = (nchunks + kCombineGroup - 1) / kCombineGroup;
+  const int gsize = min(kCombineGroup, nchunks - grp * kCombineGroup);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(tk + 1 + grp, 1u) == (unsigned)gsize - 1u;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  float* sw = mw;  // [rep][K] weights, then [rep] totals (the merge area is free again)
+  auto merge = [&](const float* src0, long qstride, int K, bool final_out, float* dst0, long dst_qstride) {
+    float* wts = sw;
+    float* tot = sw + rep * K;
+    for (int i = threadIdx.x; i < rep * K; i += blockDim.x) {
+      const int rho = i / K, k = i % K;
+      wts[i] = __ldcg(src0 + rho * qstride + (long)k * rowlen + D);
+    }
+    __syncthreads();
+    for (int rho = threadIdx.x; rho < rep; rho += blockDim.x) {
+      float M = -INFINITY;
+      for (int k = 0; k < K; ++k) M = fmaxf(M, wts[rho * K + k]);
+      float den = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        const float mk = wts[rho * K + k];
+        const float f = (mk == -INFINITY) ? 0.0f : fast_exp2(mk - M);
+        den += f * __ldcg(src0 + rho * qstride + (long)k * rowlen + D + 1);
+        wts[rho * K + k] = f;
+      }
+      tot[2 * rho] = M;
+      tot[2 * rho + 1] = den;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
+      const int rho = i / D, c = i % D;
+      const float* src = src0 + rho * qstride + c;
+      const float* w = wts + rho * K;
+      float n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
+      int k = 0;
+      for (; k + 4 <= K; k += 4) {
+        n0 += w[k] * __ldcg(src + (long)k * rowlen);
+        n1 += w[k + 1] * __ldcg(src + (long)(k + 1) * rowlen);
+        n2 += w[k + 2] * __ldcg(src + (long)(k + 2) * rowlen);
+        n3 += w[k + 3] * __ldcg(src + (long)(k + 3) * rowlen);
+      }
+      for (; k < K; ++k) n0 += w[k] * __ldcg(src + (long)k * rowlen);
+      const float num = (n0 + n1) + (n2 + n3);
+      if (final_out) {
+        const float den = tot[2 * rho + 1];
+        a.out[(hqb + rho) * D + c] = den > 0.0f ? num / den : 0.0f;
+      } else {
+        dst0[rho * dst_qstride + c] = num;
+      }
+    }
+    if (!final_out)
+      for (int rho = threadIdx.x; rho < rep; rho += blockDim.x) {
+        dst0[rho * dst_qstride + D] = tot[2 * rho];
+        dst0[rho * dst_qstride + D + 1] = tot[2 * rho + 1];
+      }
+  };
+  const float* part0 = a.work + (hqb * max_chunks + (long)grp * kCombineGroup) * rowlen;
+  if (ngroups == 1) {
+    merge(part0, (long)max_chunks * rowlen, gsize, true, nullptr, 0);
+    if (threadIdx.x == 0) tk[1 + grp] = 0u;
+    return;
+  }
+  float* g0 = a.gwork + (hqb * a.max_groups + grp) * rowlen;
+  merge(part0, (long)max_chunks * rowlen, gsize, false, g0, (long)a.max_groups * rowlen);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned prev = atomicAdd(a.tickets + bh, 1u);
-    last = (prev == (unsigned)nchunks - 1u);
+    tk[1 + grp] = 0u;
+    last = atomicAdd(tk, 1u) == (unsigned)ngroups - 1u;
   }
   __syncthreads();
   if (!last) return;
   __threadfence();
-  for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
-    const int rho = i / D, c = i % D;
-    const float* pbase = a.work + (hqb + rho) * max_chunks * (long)rowlen;
-    float M = -INFINITY;
-    for (int k = 0; k < nchunks; ++k) M = fmaxf(M, __ldcg(pbase + (long)k * rowlen + D));
-    float num = 0.0f, den = 0.0f;
-    for (int k = 0; k < nchunks; ++k) {
-      const float mk = __ldcg(pbase + (long)k * rowlen + D);
-      const float f = (mk == -INFINITY) ? 0.0f : fast_exp2(mk - M);
-      num += f * __ldcg(pbase + (long)k * rowlen + c);
-      den += f * __ldcg(pbase + (long)k * rowlen + D + 1);
-    }
-    a.out[(hqb + rho) * D + c] = den > 0.0f ? num / den : 0.0f;
-  }
-  if (threadIdx.x == 0) a.tickets[bh] = 0u;
+  merge(a.gwork + hqb * a.max_groups * rowlen, (long)a.max_groups * rowlen, ngroups, true, nullptr, 0);
+  if (threadIdx.x == 0) tk[0] = 0u;
 }
 
 }  // namespace kvq

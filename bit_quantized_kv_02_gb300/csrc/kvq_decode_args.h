@@ -31,8 +31,10 @@ struct DecodeArgs {
   float scale_log2;         // softmax scale * log2(e)
   int S, Sw;                // tokens per CTA / per warp
   int max_chunks;
-  float* work;              // [B][H*rep][max_chunks][D+2]
-  uint32_t* tickets;        // [B][H]
+  float* work;              // [B][H*rep][max_chunks][D+2] chunk partials
+  float* gwork;             // [B][H*rep][max_groups][D+2] group partials
+  int max_groups;           // ceil(max_chunks / kCombineGroup)
+  uint32_t* tickets;        // [B][H][1 + max_groups]: head ticket, then one per chunk group
   float* out;               // [B][H*rep][D]
   int* err;
   // shared-memory plan (bytes)

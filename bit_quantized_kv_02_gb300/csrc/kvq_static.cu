@@ -52,8 +52,8 @@ extern "C" kvq_status kvq_decode_attn_static(kvq_cache_t C, int layer, const voi
   if (!q || !out || (q_dtype != KVQ_F16 && q_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f)) softmax_scale = 1.0f / std::sqrt((float)C->cfg.head_dim);
   const kvq_config& c = C->cfg;
-  const size_t work_bytes = align256((size_t)c.batch * c.q_heads * C->max_chunks * (c.head_dim + 2) * 4);
-  const size_t ticket_bytes = (size_t)c.batch * c.kv_heads * 4;
+  const size_t work_bytes = align256(kvq::decode_work_floats(c.batch, c.q_heads, c.head_dim, C->max_chunks) * 4);
+  const size_t ticket_bytes = kvq::decode_ticket_words(c.batch, c.kv_heads, C->max_chunks) * 4;
   if (work_bytes + ticket_bytes > kStaticScratchBytes) {
     C->last_error = "kvq_decode_attn_static: needs " + std::to_string(work_bytes + ticket_bytes) +
                     " bytes of scratch, the static array holds " + std::to_string(kStaticScratchBytes);

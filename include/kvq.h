@@ -88,7 +88,8 @@ typedef struct {
   int max_tokens;  /* capacity per sequence, >= 1 */
   kvq_tensor_cfg k, v;
   int meta_dtype;  /* kvq_dtype of the stored zero point / step: KVQ_F16 (default) or KVQ_F32 */
-  int max_splits;  /* split-K partitions per sequence for decode; 0 = default (enough for 512-token splits) */
+  int max_splits;  /* split-K partitions per sequence for decode, <= 1024; 0 = default (about
+                      4864 / (batch * kv_heads), at least 8, at most one per 64 tokens) */
 } kvq_config;
 
 /* Byte accounting.  The first four terms follow the memory model total =
@@ -160,8 +161,9 @@ kvq_status kvq_decode_attn(kvq_cache_t cache, int layer, const void* q, int q_dt
  * runtime whose device memory is laid out once by another component, or a
  * plugin that must not call cudaMalloc.  Allocates nothing.  The source pages
  * have no counterpart of this call; it is a deployment convenience.
- *  - Needs batch * q_heads * max_chunks * (head_dim + 2) * 4 bytes (rounded up
- *    to 256) + batch * kv_heads * 4 bytes <= 16 MiB, else KVQ_ERR_BUFFER_TOO_SMALL
+ *  - Needs batch * q_heads * (max_splits + ceil(max_splits/16)) * (head_dim + 2)
+ *    * 4 bytes (rounded up to 256) + batch * kv_heads * (1 + ceil(max_splits/16))
+ *    * 4 bytes <= 16 MiB, else KVQ_ERR_BUFFER_TOO_SMALL
  *    (nothing launched; kvq_last_error says how much was needed).
  *  - The first call on a device looks up the array's device address with that
  *    device current (cudaGetSymbolAddress); make that first call before any

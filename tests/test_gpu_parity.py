@@ -173,6 +173,13 @@ def test_many_splits_and_ragged():
     run_case(wl, [3000, 1, 0, 1777], max_splits=64)
 
 
+def test_two_level_combine_long_sequence():
+    """One long sequence split into several hundred chunks: the partials merge
+    in groups of 16 and then across groups."""
+    wl = W("long", 1, 8, 1, 64, (4, 32, PC, ASYM), (4, 32, PT, ASYM), seed=12)
+    run_case(wl, [40000], max_splits=1024)
+
+
 @pytest.mark.parametrize("kc,vc", [((4, 32, PC, ASYM), (4, 32, PT, ASYM)), ((2, 16, PC, SYM), (3, 16, PC, ASYM)),
                                    ((5, 64, PT, ASYM), (6, WHOLE, PT, ASYM))])
 def test_append_equals_prefill(kc, vc):
