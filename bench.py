@@ -100,58 +100,121 @@ def ncu_traffic(workload_name: str):
     return float(t.group(1))
 
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (SM clock, max SM clock, clock
+    event reasons) for the clock sampler."""
+    SM = 1
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, dev: torch.device):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        try:
+            pr = torch.cuda.get_device_properties(dev)
+            bus = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0".encode()
+            ok = self.lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) == 0
+        except Exception:
+            ok = False
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(dev.index or 0), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("no NVML handle")
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self.reasons_fn = fn if fn is not None else self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        c = self.c
+        sm, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, c.byref(sm)) != 0:
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, c.byref(mx))
+        self.reasons_fn(self.h, c.byref(rs))
+        return float(sm.value), float(mx.value), [n for bit, n in self.REASONS.items() if rs.value & bit]
+
+
 class Clocks:
-    """nvidia-smi sampler running during the timed region."""
+    """SM clock / clock-event-reason sampler running during the timed region:
+    NVML polled from a thread every 0.2 ms (the timed regions last only
+    milliseconds), else nvidia-smi every 200 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, dev_index: int):
+    def __init__(self, dev: torch.device):
+        import threading
         self.proc = None
-        self.dev = dev_index
+        self.samples = []
+        self.switch = sys.getswitchinterval()
+        self.stop_flag = threading.Event()
+        self.thread = None
+        self.nv = None
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={dev_index}", f"--query-gpu={self.Q}",
+            nv = _Nvml(dev)
+            self.nv = nv
+
+            def loop():
+                while not self.stop_flag.is_set():
+                    r = nv.sample()
+                    if r is not None:
+                        self.samples.append(r)
+                    time.sleep(0.0002)
+
+            sys.setswitchinterval(0.0002)  # let the sampler run while the host waits on the GPU
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            self.source = "nvml, polled every 0.2 ms"
+            return
+        except Exception:
+            self.thread = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={dev.index or 0}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi 200 ms"
         except Exception:
             self.proc = None
 
+    def poll(self):
+        """One sample from the calling thread (used while the GPU runs a step)."""
+        if self.nv is not None:
+            r = self.nv.sample()
+            if r is not None:
+                self.samples.append(r)
+
     def stop(self):
-        if not self.proc:
-            return None
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except Exception:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=5)
+            sys.setswitchinterval(self.switch)
+        elif self.proc:
+            self.proc.terminate()
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    self.samples.append((float(f[1]), float(f[2]),
+                                         [n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")]))
+                except ValueError:
+                    continue
+        else:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)), "reasons": sorted(reasons),
-                "samples": len(sm)}
-
-
-def make_event(external: bool):
-    if external:
-        try:
-            return torch.cuda.Event(enable_timing=True, external=True)
-        except TypeError:
+        if not self.samples:
             return None
-    return torch.cuda.Event(enable_timing=True)
+        sm = [x[0] for x in self.samples]
+        reasons = sorted({r for x in self.samples for r in x[2]})
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(x[1] for x in self.samples)),
+                "reasons": reasons, "samples": len(sm), "source": self.source}
 
 
 def run_ours(args, rank, world):
@@ -187,25 +250,29 @@ def run_ours(args, rank, world):
     out = torch.empty((L, B, Hq, D), dtype=torch.float32, device=dev)
     out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
     scale = float(np.float32(1.0 / np.sqrt(D)))
-    ev_ext = [(make_event(True), make_event(True)) for _ in range(L)]
-    in_graph_timing = all(a is not None for a, _ in ev_ext)
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
-    graph = torch.cuda.CUDAGraph()
     kin.copy_(kin_all[0])
     qin.copy_(q_all[0])
     torch.cuda.synchronize()
+    # the step: per layer kvq_append then kvq_decode_attn; consecutive launches
+    # overlap their launch latency (programmatic dependent launch), so the graph
+    # holds no timing events between them
+    graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for l in range(L):
             cache.kvq_append(l, kin[l, 0], kin[l, 1], stream=stream)
-            if in_graph_timing:
-                ev_ext[l][0].record(stream)
             cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
-            if in_graph_timing:
-                ev_ext[l][1].record(stream)
+    # the decode kernel alone: the step's L decode launches back to back (same
+    # inputs, same cache state), timed as a whole after its own L2 flush
+    graph_dec = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_dec, stream=stream):
+        for l in range(L):
+            cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
     launches_per_step = 2 * L
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = None
 
     def traffic():
         cache.kvq_refresh_lens(stream)
@@ -226,35 +293,38 @@ def run_ours(args, rank, world):
             if e2e:
                 out_host.copy_(out, non_blocking=True)
             e1.record(stream)
+        if clocks:
+            clocks.poll()  # the GPU is running the step now
+        stream.synchronize()
+        return e0.elapsed_time(e1)
+
+    def decode_pass():
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            graph_dec.replay()
+            e1.record(stream)
+        if clocks:
+            clocks.poll()
         stream.synchronize()
         return e0.elapsed_time(e1)
 
     # warm-up (untimed)
     for s in range(warm):
         one_step(s, False)
+        decode_pass()
     kdist.barrier()
-    clocks = Clocks(dev.index) if rank == 0 else None
+    clocks = Clocks(dev) if rank == 0 else None
     t_steps, t_decode, tot_bytes, tot_tokens = 0.0, 0.0, 0.0, 0.0
     for s in range(warm, nsteps):
         t_steps += one_step(s, False)
-        if in_graph_timing:
-            t_decode += sum(a.elapsed_time(b) for a, b in ev_ext)
         by, tk = traffic()
         tot_bytes += by
         tot_tokens += tk
+        t_decode += decode_pass()
     clk = clocks.stop() if clocks else None
+    clocks = None
     kdist.barrier()
-    # decode kernel alone when the graph could not hold timing events: eager launches, same stream
-    if not in_graph_timing:
-        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for l in range(L):
-            with torch.cuda.stream(stream):
-                flush.zero_()
-                ea.record(stream)
-                cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
-                eb.record(stream)
-            stream.synchronize()
-            t_decode += ea.elapsed_time(eb) * steps
     # end-to-end: host inputs -> device -> host outputs, same graph
     t_e2e = 0.0
     for s in range(e2e_steps):
@@ -297,8 +367,9 @@ def run_ours(args, rank, world):
                          else "fallback",
                          "kernel": "decode_kernel", "bytes_per_launch": round(dec_bytes_per_launch),
                          "us_per_launch": round(dec_ms_per_launch * 1e3, 3),
-                         "timing": "events in graph around each decode launch" if in_graph_timing
-                         else "events around eager decode launches"},
+                         "timing": "CUDA events on the launching stream around a graph of the step's "
+                                   f"{L} decode launches (after an L2 flush), once per timed step",
+                         "decode_launches_timed": L * steps},
             "gpu_launches": launches_per_step * steps,
             "e2e": {"value": round(bytes_e2e_all / (t_e2e_max * 1e-3) / 1e9, 2) if e2e_steps else None,
                     "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,

@@ -122,8 +122,8 @@ size_t carve(const kvq_config& c, kvq_cache* C) {
   off += align256((size_t)L * B * 4);
   size_t smax_off = off;
   off += align256((size_t)2 * L * B * H * 4);
-  size_t at_off = off;
-  off += align256((size_t)B * 4);
+  size_t hl_off = off;
+  off += align256((size_t)L * B * H * 4);
   const int mc = max_chunks_of(c, tcap);
   size_t dt_off = off;
   off += align256(decode_ticket_words(B, H, mc) * 4);
@@ -138,7 +138,7 @@ size_t carve(const kvq_config& c, kvq_cache* C) {
     C->max_chunks = mc;
     C->d_lens = reinterpret_cast<int32_t*>(C->base + lens_off);
     C->d_smax = reinterpret_cast<uint32_t*>(C->base + smax_off);
-    C->d_append_tickets = reinterpret_cast<uint32_t*>(C->base + at_off);
+    C->d_head_lens = reinterpret_cast<int32_t*>(C->base + hl_off);
     C->d_decode_tickets = reinterpret_cast<uint32_t*>(C->base + dt_off);
     C->d_err = reinterpret_cast<int*>(C->base + err_off);
     C->d_work = reinterpret_cast<float*>(C->base + work_off);
@@ -353,8 +353,9 @@ kvq_status kvq_set_decode_plan(kvq_cache_t C, int plan_tokens) {
 }
 
 kvq_status kvq_set_decode_kernel(kvq_cache_t C, int which) {
-  if (!C || (which != 0 && which != 1)) return KVQ_ERR_INVALID_ARG;
-  C->generic_decode = which;
+  if (!C || which < 0 || which > 3) return KVQ_ERR_INVALID_ARG;
+  C->generic_decode = which & 1;
+  C->global_combine = (which >> 1) & 1;
   return cuda_status(C, decode_setup(C));
 }
 

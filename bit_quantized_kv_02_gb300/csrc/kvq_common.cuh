@@ -32,8 +32,10 @@ constexpr int kWarps = 4;         // warps per decode CTA
 constexpr int kMaxBatch = 1024;   // sequences per cache
 constexpr int kCombineGroup = 16; // split-K partials merged per combine step
 // At most kMaxSplits / kCombineGroup = 64 group partials, so the combine's
-// weights (rep * 66 floats) always fit the CTA merge area (rep * 4 * (D + 2)).
+// staging (rep * (2 * 64 + 2) floats) always fits the CTA merge area
+// (rep * 4 * (D + 2) floats).
 constexpr int kMaxSplits = 1024;
+constexpr int kMaxCluster = 8;    // splits merged inside one thread-block cluster (portable size)
 
 // split-K workspace: chunk partials + group partials, and combine tickets
 inline int combine_groups(int max_chunks) { return (max_chunks + kCombineGroup - 1) / kCombineGroup; }
@@ -190,66 +192,30 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+// 16-byte asynchronous global -> shared copy that bypasses L1; completion is
+// tracked per thread in commit groups (cp.async.commit_group / wait_group).
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// bytes (a multiple of 16, both addresses 16-byte aligned) copied by the 32
+// lanes of a warp, 16 bytes per lane and step
+__device__ __forceinline__ void warp_copy(void* dst, const void* src, int bytes, int lane) {
+  for (int o = lane * 16; o < bytes; o += 512)
+    cp_async16(static_cast<char*>(dst) + o, static_cast<const char*>(src) + o);
 }
 
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-// 1-D bulk copy global -> shared (TMA engine), completion counted on `bar`.
-// dst, src 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
-  return t;
-}
-
-// Bounded wait on an mbarrier phase: gives up after ~1 s, records the failure
-// in *err and returns false.  Never spins forever.  The slow path is out of
-// line so the common case (data already landed) costs one test.
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, int* err) {
-  uint64_t t0 = global_timer_ns();
-  for (int it = 0; it < (1 << 30); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255) == 255 && global_timer_ns() - t0 > 1000000000ull) break;
-  }
-  if (err) atomicExch(err, 1);
-  return false;
-}
-
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  return mbar_wait_slow(bar, parity, err);
-}
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while the previous kernel of the stream still runs;
+// pdl_wait() returns once that kernel has completed and its writes are
+// visible (immediately for an ordinary launch), and pdl_trigger() lets the next
+// such kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 __device__ __forceinline__ void mma_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                           uint32_t b1) {

@@ -101,10 +101,19 @@ cudaError_t decode_setup(kvq_cache* C) {
   if (P.smem > 227 * 1024) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.smem);
   if (e != cudaSuccess) return e;
+  // the same (largest) shared-memory carve-out as the append kernel, so that
+  // alternating append / decode launches need no L1 / shared reconfiguration
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kWarps * 32, P.smem);
   if (e != cudaSuccess) return e;
   C->dec_smem = P.smem;
   C->dec_occ = std::max(occ, 1);
+  // the cluster combine keeps the CTA partial and its staging after the four
+  // warp partials in the merge area (the per-warp regions)
+  const int rep = C->cfg.q_heads / C->cfg.kv_heads, rowlen = C->cfg.head_dim + 2;
+  const long need = (5L * rep * rowlen + 2L * rep * kMaxCluster + rep) * 4;
+  C->dec_cluster_ok = need <= 4L * P.a.warp_bytes && !C->global_combine;
   return cudaSuccess;
 }
 
@@ -141,52 +150,15 @@ static int choose_split(const kvq_cache* C, const int32_t* lens, int unit, int s
   return best;
 }
 
-cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
-                          cudaStream_t st, int* launches) {
-  Plan P;
+// Plan one decode launch on the host length mirror, raised to the plan hint (a
+// launch planned for the hint stays valid while the cache grows up to it):
+// split size, grid, and how the split-K partials merge.
+static cudaError_t plan_launch(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out, Plan* P,
+                               dim3* grid) {
   int occ = 1;
-  cudaError_t e = make_plan(C, layer, &P, &occ);
+  cudaError_t e = make_plan(C, layer, P, &occ);
   if (e != cudaSuccess) return e;
-  DecodeArgs& a = P.a;
-  const kvq_config& cfg = C->cfg;
-  int unit = kTile;
-  if (C->k.axis == 1) unit = std::max(unit, C->k.group);
-  if (C->v.axis == 1) unit = std::max(unit, C->v.group);
-  // plan on the host length mirror, raised to the plan hint (a launch planned
-  // for the hint stays valid while the cache grows up to it)
-  std::vector<int32_t> plan(C->lens.begin() + (long)layer * cfg.batch, C->lens.begin() + (long)(layer + 1) * cfg.batch);
-  for (auto& x : plan) x = std::max(x, (int32_t)std::min(C->plan_tokens, C->cfg.max_tokens));
-  const int32_t* lens = plan.data();
-  const int slots = C->sm_count * occ;
-  a.S = choose_split(C, lens, unit, slots, C->max_chunks);
-  a.Sw = a.S / kWarps;
-  int maxn = 0;
-  for (int b = 0; b < cfg.batch; ++b) maxn = std::max(maxn, (int)lens[b]);
-  const int nch = std::max(1, (maxn + a.S - 1) / a.S);
-  a.q = q;
-  a.q_f32 = q_f32;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.out = out;
-  dim3 grid(nch, cfg.kv_heads, cfg.batch);
-  void* args[] = {&a};
-  e = cudaLaunchKernel(C->dec_fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
-  ++*launches;
-  return e;
-}
-
-// Same plan and kernel as launch_decode, with the split-K partials and the
-// combine tickets placed in caller-chosen scratch (used by the entry point
-// whose scratch is a static device array).
-cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
-                                  cudaStream_t st, int* launches, float* work, uint32_t* tickets) {
-  Plan P;
-  int occ = 1;
-  cudaError_t e = make_plan(C, layer, &P, &occ);
-  if (e != cudaSuccess) return e;
-  DecodeArgs& a = P.a;
-  a.work = work;
-  a.gwork = work + (size_t)C->cfg.batch * C->cfg.q_heads * C->max_chunks * (C->cfg.head_dim + 2);
-  a.tickets = tickets;
+  DecodeArgs& a = P->a;
   const kvq_config& cfg = C->cfg;
   int unit = kTile;
   if (C->k.axis == 1) unit = std::max(unit, C->k.group);
@@ -199,13 +171,48 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   int maxn = 0;
   for (int b = 0; b < cfg.batch; ++b) maxn = std::max(maxn, (int)plan[b]);
   const int nch = std::max(1, (maxn + a.S - 1) / a.S);
+  // up to kMaxCluster splits of a (sequence, head) form one thread-block
+  // cluster and merge through distributed shared memory; more go through the
+  // global workspace and atomic tickets
+  // (only when the whole grid is resident at once: with several waves, CTAs
+  // that wait for their cluster would hold slots that later CTAs need)
+  const long ctas = (long)nch * cfg.kv_heads * cfg.batch;
+  a.csize = (C->dec_cluster_ok && nch <= kMaxCluster && ctas <= slots) ? nch : 0;
   a.q = q;
   a.q_f32 = q_f32;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = out;
-  dim3 grid(nch, cfg.kv_heads, cfg.batch);
+  *grid = dim3(nch, cfg.kv_heads, cfg.batch);
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
+                          cudaStream_t st, int* launches) {
+  Plan P;
+  dim3 grid;
+  cudaError_t e = plan_launch(C, layer, q, q_f32, scale, out, &P, &grid);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&P.a};
+  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), C->dec_smem, st, args, P.a.csize);
+  ++*launches;
+  return e;
+}
+
+// Same plan and kernel as launch_decode, with the split-K partials and the
+// combine tickets placed in caller-chosen scratch (used by the entry point
+// whose scratch is a static device array).
+cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
+                                  cudaStream_t st, int* launches, float* work, uint32_t* tickets) {
+  Plan P;
+  dim3 grid;
+  cudaError_t e = plan_launch(C, layer, q, q_f32, scale, out, &P, &grid);
+  if (e != cudaSuccess) return e;
+  DecodeArgs& a = P.a;
+  a.work = work;
+  a.gwork = work + (size_t)C->cfg.batch * C->cfg.q_heads * C->max_chunks * (C->cfg.head_dim + 2);
+  a.tickets = tickets;
   void* args[] = {&a};
-  e = cudaLaunchKernel(C->dec_fn, grid, dim3(kWarps * 32), args, C->dec_smem, st);
+  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), C->dec_smem, st, args, a.csize);
   ++*launches;
   return e;
 }

@@ -2,14 +2,17 @@
 //
 // One CTA = one (sequence, kv head, token chunk); 4 warps, each an independent
 // flash-decoding pass over a contiguous, group-aligned sub-range, merged at the
-// end of the CTA; the last CTA of a (sequence, kv head) merges all chunks
-// (log-sum-exp combine) behind an atomic ticket, so no kernel ever waits on
-// another CTA.
+// end of the CTA.  The chunks of a (sequence, kv head) then merge their
+// partials (log-sum-exp combine): inside one thread-block cluster through
+// distributed shared memory when the grid is a single wave of at most 8 chunks
+// per head, otherwise in the global workspace behind atomic tickets (the last
+// arriving CTA merges; no CTA ever waits for another).
 //
 // Per 16-token tile a warp:
 //   1. waits for its stage: packed codes + metadata copied global -> shared by
-//      the TMA engine (cp.async.bulk, mbarrier completion, bounded waits), and
-//      turns the stage's metadata into fp32 (step, folded zero) pairs once;
+//      16-byte cp.async from all 32 lanes (completion tracked per lane in commit
+//      groups, a ring of 2 or 4 stages), and turns the stage's metadata into
+//      fp32 (step, folded zero) pairs once;
 //   2. QK: converts the key codes of each 16-channel chunk to exact fp16
 //      operands in registers (one rotate + one LOP3 per code pair and bit
 //      plane: the code lands in the top mantissa bits of an fp16 whose
@@ -31,6 +34,8 @@
 // section "Kuantisasi dapat memindahkan pekerjaan ke decode path"); the GPU
 // design here is this library's own.
 #pragma once
+
+#include <cooperative_groups.h>
 
 #include "kvq_decode_args.h"
 
@@ -276,15 +281,34 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const int rep = CFG::rep(a), H = a.H, S = a.S;
+  pdl_wait();  // the cache and the query are complete
+  const int hq0 = h * rep;
+  // the query and the largest steps are requested before the length, so the
+  // three loads are in flight together
+  constexpr int QPT = D / 16;  // query values per thread at rep 8
+  float qv[QPT];
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    const int i = threadIdx.x + u * 128;
+    const long qi = ((long)b * H * rep + hq0) * D + i;
+    qv[u] = 0.0f;
+    if (i < rep * D)
+      qv[u] = a.q_f32 ? reinterpret_cast<const float*>(a.q)[qi] : __half2float(reinterpret_cast<const __half*>(a.q)[qi]);
+  }
+  const float smax_k = __uint_as_float(a.smax_k[(long)b * H + h]);
+  const float smax_v = __uint_as_float(a.smax_v[(long)b * H + h]);
   const int n = a.lens[b];
   const int nchunks = (n + S - 1) / S;
-  const int hq0 = h * rep;
-  if (n == 0) {
-    if (chunk == 0)
-      for (int i = threadIdx.x; i < rep * D; i += blockDim.x) a.out[((long)b * H * rep + hq0) * D + i] = 0.0f;
-    return;
+  // (in a cluster launch every CTA takes part in the merge: splits past the
+  // sequence's end just contribute empty partials)
+  if (!a.csize) {
+    if (n == 0) {
+      if (chunk == 0)
+        for (int i = threadIdx.x; i < rep * D; i += blockDim.x) a.out[((long)b * H * rep + hq0) * D + i] = 0.0f;
+      return;
+    }
+    if (chunk >= nchunks) return;
   }
-  if (chunk >= nchunks) return;
 
   // ---- tensor formats (constants in a compile-time configuration)
   const int kbits = CFG::kbits(a), ksym = CFG::ksym(a), kf32 = CFG::kf32(a), kwhole = CFG::kwhole(a);
@@ -308,29 +332,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   float2* canV = canK + CFG::canon_k(a);                                   // canonical value metadata
   float* wbias = reinterpret_cast<float*>(canV + CFG::canon_v(a));         // [8] per-channel key bias
   unsigned char* stages = wbase + CFG::stage_off(a);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + (stage_bytes << lg_ns));
-
-  for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
-    const long qi = ((long)b * H * rep + hq0) * D + i;
-    qs[i] = (a.q_f32 ? reinterpret_cast<const float*>(a.q)[qi] : __half2float(reinterpret_cast<const __half*>(a.q)[qi])) *
-            a.scale_log2;
-  }
-  __syncthreads();
-  if (k_token) {
-    const int Gk = kwhole ? D : kG;  // within one head a whole-vector group spans all D channels
-    for (int i = threadIdx.x; i < kgpt * rep; i += blockDim.x) {
-      const int jg = i / rep, rho = i % rep;
-      float s = 0.0f;
-      for (int c = jg * Gk; c < (jg + 1) * Gk; ++c) s += qs[rho * D + c];
-      qg[jg * rep + rho] = s;
-    }
-  }
-  for (int i = lane; i < CFG::barea_bytes(a) / 4; i += 32) barea[i] = 0u;
-  if (lane < 8) wbias[lane] = 0.0f;
-  if (lane == 0)
-    for (int s = 0; s < ns; ++s) mbar_init(&bars[s], 1);
-  fence_mbar_init();
-  __syncthreads();
 
   // ---- this warp's token range and its copy sources
   const int w0 = chunk * S + warp * a.Sw;
@@ -351,6 +352,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   const int kgmask = k_token ? 0 : kG - 1;
   const int vgmask = VAXIS == 0 ? 0 : vG - 1;
 
+  // stage i of this warp's range: every lane copies its 16-byte pieces
   auto issue = [&](int i) {
     const int s = i & (ns - 1);
     const int t0 = w0 + i * kTile;
@@ -379,15 +381,40 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
       }
       bytes += vc_bytes + vmb_i;
     }
-    mbar_expect_tx(&bars[s], bytes);
-    if (kp) bulk_g2s(st + st_kc, kc_src + (long)i * kc_bytes, kc_bytes, &bars[s]);
-    if (kmb_i) bulk_g2s(st + st_km, kms, kmb_i, &bars[s]);
-    if (vp) bulk_g2s(st + st_vc, vc_src + (long)i * vc_bytes, vc_bytes, &bars[s]);
-    if (vmb_i) bulk_g2s(st + st_vm, vms, vmb_i, &bars[s]);
+    if (kp) warp_copy(st + st_kc, kc_src + (long)i * kc_bytes, kc_bytes, lane);
+    if (kmb_i) warp_copy(st + st_km, kms, kmb_i, lane);
+    if (vp) warp_copy(st + st_vc, vc_src + (long)i * vc_bytes, vc_bytes, lane);
+    if (vmb_i) warp_copy(st + st_vm, vms, vmb_i, lane);
   };
 
-  if (lane == 0)
-    for (int i = 0; i < min(ntl, ns); ++i) issue(i);
+  // the first stages go out before the query set-up, so their DRAM latency
+  // overlaps it
+  // (one commit group per stage, empty past the range's end, so that the
+  // group of tile i is always the (i+1)-th oldest)
+  for (int i = 0; i < ns; ++i) {
+    if (i < ntl) issue(i);
+    cp_async_commit();
+  }
+
+#pragma unroll
+  for (int u = 0; u < QPT; ++u) {
+    const int i = threadIdx.x + u * 128;
+    if (i < rep * D) qs[i] = qv[u] * a.scale_log2;
+  }
+  __syncthreads();
+  if (k_token) {
+    const int Gk = kwhole ? D : kG;  // within one head a whole-vector group spans all D channels
+    for (int i = threadIdx.x; i < kgpt * rep; i += blockDim.x) {
+      const int jg = i / rep, rho = i % rep;
+      float s = 0.0f;
+      for (int c = jg * Gk; c < (jg + 1) * Gk; ++c) s += qs[rho * D + c];
+      qg[jg * rep + rho] = s;
+    }
+  }
+  for (int i = lane; i < CFG::barea_bytes(a) / 4; i += 32) barea[i] = 0u;
+  if (lane < 8) wbias[lane] = 0.0f;
+  __syncthreads();
+
 
   // ---- per-warp state
   float m_run[SL::N], l_run[SL::N];
@@ -435,7 +462,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
   const int E_unit = norm_exp(qmax);
-  const int E_chan = k_token ? E_unit : norm_exp(qmax * __uint_as_float(a.smax_k[(long)b * H + h]));
+  const int E_chan = k_token ? E_unit : norm_exp(qmax * smax_k);
   int Ek = E_unit;
   bool qb_unit = false;
   if (k_token) {
@@ -444,7 +471,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
     load_b();
   }
   // value step normalisation: every folded p * step lies below 2^15
-  const int E_v = VAXIS == 0 ? norm_exp(__uint_as_float(a.smax_v[bh])) : 0;
+  const int E_v = VAXIS == 0 ? norm_exp(smax_v) : 0;
   const float sc_v = exp2i(E_v), inv_sc_v = exp2i(-E_v);
   const int hl = g & 1;
   // per-lane rows into the canonical metadata
@@ -461,15 +488,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   const float2* cv_t1 = canV + (tk0 + 1) * gs_v;
   const float2* cv_t2 = canV + (tk0 + 8) * gs_v;
   const float2* cv_t3 = canV + (tk0 + 9) * gs_v;
-  bool failed = false;
 
   // One 16-token tile.  FAST: the tile is full and both its keys and values are
   // packed (the bulk of every range), so the tail and partial-tile checks fold away.
-  auto tile_body = [&](const int i, auto stag, auto ftag) -> bool {
+  auto tile_body = [&](const int i, auto stag, auto ftag) {
     constexpr bool FAST = decltype(ftag)::value != 0;
     const int s = stag.get(i);
     const int t0 = w0 + i * kTile;
-    if (!mbar_wait_bounded(&bars[s], (uint32_t)((i >> lg_ns) & 1), a.err)) return false;
+    // ns groups are younger than tile i's: wait until at most ns - 1 are
+    // pending, then the warp barrier makes every lane's copies visible
+    if (CFG::kStaticStages == 4 || (CFG::kStaticStages == 0 && lg_ns == 2)) cp_async_wait<3>();
+    else cp_async_wait<1>();
+    __syncwarp();
     const unsigned char* st = stages + s * stage_bytes;
     const bool kp = FAST || t0 < sealed_k, vp = FAST || t0 < sealed_v;
     const bool vflush = VAXIS == 1 && vp && ((t0 + kTile) & vgmask) == 0;
@@ -793,12 +823,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
       }
     }
 
-    __syncwarp();
-    if (lane == 0 && i + ns < ntl) {
-      fence_proxy_async();
-      issue(i + ns);
-    }
-    return true;
+    __syncwarp();  // every lane is done with stage s before it is refilled
+    if (i + ns < ntl) issue(i + ns);
+    cp_async_commit();
   };
 
   {
@@ -809,20 +836,24 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
     int i = 0;
     constexpr int NSC = CFG::kStaticStages;
     if constexpr (NSC == 4) {
-      for (; i + 4 <= nfast && !failed; i += 4)
-        failed = !(tile_body(i, StageC<0>{}, IntC<1>{}) && tile_body(i + 1, StageC<1>{}, IntC<1>{}) &&
-                   tile_body(i + 2, StageC<2>{}, IntC<1>{}) && tile_body(i + 3, StageC<3>{}, IntC<1>{}));
+      for (; i + 4 <= nfast; i += 4) {
+        tile_body(i, StageC<0>{}, IntC<1>{});
+        tile_body(i + 1, StageC<1>{}, IntC<1>{});
+        tile_body(i + 2, StageC<2>{}, IntC<1>{});
+        tile_body(i + 3, StageC<3>{}, IntC<1>{});
+      }
     } else if constexpr (NSC == 2) {
-      for (; i + 2 <= nfast && !failed; i += 2)
-        failed = !(tile_body(i, StageC<0>{}, IntC<1>{}) && tile_body(i + 1, StageC<1>{}, IntC<1>{}));
+      for (; i + 2 <= nfast; i += 2) {
+        tile_body(i, StageC<0>{}, IntC<1>{});
+        tile_body(i + 1, StageC<1>{}, IntC<1>{});
+      }
     }
-    for (; i < nfast && !failed; ++i) failed = !tile_body(i, StageR{ns - 1}, IntC<1>{});
-    for (; i < ntl && !failed; ++i) failed = !tile_body(i, StageR{ns - 1}, IntC<0>{});
+    for (; i < nfast; ++i) tile_body(i, StageR{ns - 1}, IntC<1>{});
+    for (; i < ntl; ++i) tile_body(i, StageR{ns - 1}, IntC<0>{});
   }
-  if (failed && lane == 0) {
-    // give copies still in flight a bounded chance to land before the CTA exits
-    for (int s = 0; s < min(ntl, ns); ++s) mbar_wait_bounded(&bars[s], 0u, nullptr);
-  }
+  cp_async_wait<0>();  // (only empty groups remain) before the stages are reused
+
+  pdl_trigger();  // only the merge and the combine remain: the next kernel may start launching
 
   // ---- warp epilogue: complete l and the per-token value zero-point sums
 #pragma unroll
@@ -909,7 +940,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
     }
   }
   __syncthreads();
-  // CTA merge -> chunk partial in the workspace
+  // CTA merge -> chunk partial in the workspace (cluster launch: in shared
+  // memory after the four warp partials)
+  float* part = mw + kWarps * rep * rowlen;
   const long hqb = (long)b * H * rep + hq0;
   const int max_chunks = a.max_chunks;
   for (int i = threadIdx.x; i < rep * rowlen; i += blockDim.x) {
@@ -927,7 +960,50 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
         acc += f * mw[(w * rep + rho) * rowlen + c];
       }
     }
-    a.work[((hqb + rho) * max_chunks + chunk) * rowlen + c] = acc;
+    if (a.csize) part[rho * rowlen + c] = acc;
+    else a.work[((hqb + rho) * max_chunks + chunk) * rowlen + c] = acc;
+  }
+  if (a.csize) {
+    // Cluster merge: the splits of this (sequence, head) are the CTAs of one
+    // cluster; each CTA reads every CTA's partial through distributed shared
+    // memory and writes its share of the output columns.
+    namespace cg = cooperative_groups;
+    cg::cluster_group cl = cg::this_cluster();
+    const int K = a.csize;
+    const int crank = (int)cl.block_rank();
+    float* cw = part + rep * rowlen;  // [rep][K] m_k, then weights
+    float* cl_l = cw + rep * K;       // [rep][K] l_k
+    float* cden = cl_l + rep * K;     // [rep]
+    cl.sync();  // every partial of the cluster is complete and visible
+    for (int i = threadIdx.x; i < rep * K; i += blockDim.x) {
+      const int rho = i / K, k = i - rho * K;
+      const float* rp = cl.map_shared_rank(part, k);
+      cw[i] = rp[rho * rowlen + D];
+      cl_l[i] = rp[rho * rowlen + D + 1];
+    }
+    __syncthreads();
+    for (int rho = threadIdx.x; rho < rep; rho += blockDim.x) {
+      float M = -INFINITY;
+      for (int k = 0; k < K; ++k) M = fmaxf(M, cw[rho * K + k]);
+      float den = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        const float mk = cw[rho * K + k];
+        const float f = (mk == -INFINITY) ? 0.0f : fast_exp2(mk - M);
+        den += f * cl_l[rho * K + k];
+        cw[rho * K + k] = f;
+      }
+      cden[rho] = den;
+    }
+    __syncthreads();
+    for (int i = crank * blockDim.x + threadIdx.x; i < rep * D; i += K * blockDim.x) {
+      const int rho = i / D, c = i - rho * D;
+      float num = 0.0f;
+      for (int k = 0; k < K; ++k) num += cw[rho * K + k] * cl.map_shared_rank(part, k)[rho * rowlen + c];
+      const float den = cden[rho];
+      a.out[(hqb + rho) * D + c] = den > 0.0f ? num / den : 0.0f;
+    }
+    cl.sync();  // no CTA leaves while others may still read its partial
+    return;
   }
   // Two-level combine behind atomic tickets (no CTA ever waits): the last CTA
   // of each group of up to kCombineGroup chunks merges the group's partials;
@@ -944,13 +1020,19 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   __syncthreads();
   if (!last) return;
   __threadfence();
-  float* sw = mw;  // [rep][K] weights, then [rep] totals (the merge area is free again)
+  float* sw = mw;  // combine scratch (the merge area is free again)
+  // Merge K partials (m_k, l_k, O_k) per query: the (m, l) pairs are staged in
+  // shared memory by all threads at once, and every output column loads its K
+  // partial values as independent, unrolled loads.
   auto merge = [&](const float* src0, long qstride, int K, bool final_out, float* dst0, long dst_qstride) {
-    float* wts = sw;
-    float* tot = sw + rep * K;
+    float* wts = sw;                 // [rep][K] m_k, then weights
+    float* lks = sw + rep * K;       // [rep][K] l_k
+    float* tot = sw + 2 * rep * K;   // [rep][2] (M, den)
     for (int i = threadIdx.x; i < rep * K; i += blockDim.x) {
-      const int rho = i / K, k = i % K;
-      wts[i] = __ldcg(src0 + rho * qstride + (long)k * rowlen + D);
+      const int rho = i / K, k = i - rho * K;
+      const float* e = src0 + rho * qstride + (long)k * rowlen + D;
+      wts[i] = __ldcg(e);
+      lks[i] = __ldcg(e + 1);
     }
     __syncthreads();
     for (int rho = threadIdx.x; rho < rep; rho += blockDim.x) {
@@ -960,7 +1042,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
       for (int k = 0; k < K; ++k) {
         const float mk = wts[rho * K + k];
         const float f = (mk == -INFINITY) ? 0.0f : fast_exp2(mk - M);
-        den += f * __ldcg(src0 + rho * qstride + (long)k * rowlen + D + 1);
+        den += f * lks[rho * K + k];
         wts[rho * K + k] = f;
       }
       tot[2 * rho] = M;
@@ -968,19 +1050,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
     }
     __syncthreads();
     for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
-      const int rho = i / D, c = i % D;
+      const int rho = i / D, c = i - rho * D;
       const float* src = src0 + rho * qstride + c;
       const float* w = wts + rho * K;
-      float n0 = 0.f, n1 = 0.f, n2 = 0.f, n3 = 0.f;
-      int k = 0;
-      for (; k + 4 <= K; k += 4) {
-        n0 += w[k] * __ldcg(src + (long)k * rowlen);
-        n1 += w[k + 1] * __ldcg(src + (long)(k + 1) * rowlen);
-        n2 += w[k + 2] * __ldcg(src + (long)(k + 2) * rowlen);
-        n3 += w[k + 3] * __ldcg(src + (long)(k + 3) * rowlen);
+      float num = 0.0f;
+      for (int k0 = 0; k0 < K; k0 += kCombineGroup) {
+        float v[kCombineGroup];
+#pragma unroll
+        for (int u = 0; u < kCombineGroup; ++u) v[u] = (k0 + u < K) ? __ldcg(src + (long)(k0 + u) * rowlen) : 0.0f;
+#pragma unroll
+        for (int u = 0; u < kCombineGroup; ++u)
+          if (k0 + u < K) num += w[k0 + u] * v[u];
       }
-      for (; k < K; ++k) n0 += w[k] * __ldcg(src + (long)k * rowlen);
-      const float num = (n0 + n1) + (n2 + n3);
       if (final_out) {
         const float den = tot[2 * rho + 1];
         a.out[(hqb + rho) * D + c] = den > 0.0f ? num / den : 0.0f;

@@ -34,13 +34,15 @@ struct DecodeArgs {
   float* work;              // [B][H*rep][max_chunks][D+2] chunk partials
   float* gwork;             // [B][H*rep][max_groups][D+2] group partials
   int max_groups;           // ceil(max_chunks / kCombineGroup)
+  int csize;                // > 0: the grid's x dimension forms clusters of csize CTAs (all splits of one
+                            // sequence and head) that merge through distributed shared memory
   uint32_t* tickets;        // [B][H][1 + max_groups]: head ticket, then one per chunk group
   float* out;               // [B][H*rep][D]
   int* err;
   // shared-memory plan (bytes)
   int lg_nstages, stage_bytes;
   int st_kc, st_km, st_vc, st_vm;  // offsets inside a stage
-  int warp_bytes;           // per-warp region: B operand + canonical metadata + stages + barriers
+  int warp_bytes;           // per-warp region: B operand + canonical metadata + stages
   int barea_bytes;
   int canon_k, canon_v;     // canonical (step, zero') entries per warp for keys / values
   int stage_off;            // offset of the stage ring inside the per-warp region
@@ -76,7 +78,7 @@ __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, in
   L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : D;
   L.canon_v = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) : D;
   L.stage_off = dl_round(L.barea_bytes + (L.canon_k + L.canon_v) * 8 + 32, 128);
-  L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns) + (8 << L.lg_ns), 128);
+  L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns), 128);
   const int merge_bytes = 4 * rep * (D + 2) * 4;
   if (L.warp_bytes * 4 < merge_bytes) L.warp_bytes = dl_round((merge_bytes + 3) / 4, 128);
   L.head_bytes = dl_round((rep * D + (kaxis == 0 ? kgpt * rep : 0)) * 4, 128);

@@ -15,7 +15,7 @@ struct kvq_cache {
   kvq::TensorLayout k, v;
   int32_t* d_lens = nullptr;            // [layers][batch]
   uint32_t* d_smax = nullptr;           // [2][layers][batch][kv_heads] largest step (float bits), K then V
-  uint32_t* d_append_tickets = nullptr; // [batch]
+  int32_t* d_head_lens = nullptr;       // [layers][batch][kv_heads] per-head copies of the lengths (append)
   uint32_t* d_decode_tickets = nullptr; // [batch][kv_heads]
   int* d_err = nullptr;                 // device error word
   float* d_work = nullptr;              // split-K partials [batch][q_heads][max_chunks][head_dim + 2]
@@ -28,11 +28,40 @@ struct kvq_cache {
   int plan_tokens = 0;  // decode split plan assumes at least this many tokens per sequence
   size_t dec_smem = 0;  // dynamic shared memory of the decode kernel
   int dec_occ = 1;      // resident decode CTAs per SM
+  int dec_cluster_ok = 0;  // split-K partials may merge inside a thread-block cluster
+  int global_combine = 0;  // 1: always merge split-K partials through the global workspace
   void* dec_fn = nullptr;  // decode kernel in use (compile-time specialisation or generic)
   int generic_decode = 0;  // 1: always use the generic (runtime-format) decode kernel
 };
 
 namespace kvq {
+
+// Launch with programmatic stream serialisation: the kernel's CTAs may be
+// scheduled while the previous kernel of the stream finishes; every such
+// kernel calls pdl_wait() before it touches global memory.
+// cluster_x > 0 also groups the grid's x dimension into clusters of that size.
+inline cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, void** args,
+                              int cluster_x = 0) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (cluster_x > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster_x;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    na = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
 
 struct LensArg {
   int v[kMaxBatch];

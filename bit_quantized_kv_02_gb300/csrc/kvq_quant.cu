@@ -272,9 +272,14 @@ __global__ void prefill_token_kernel(QuantArgs a) {
     for (int hh = 0; hh < nh; ++hh) atomic_max_pos(a.smax + (long)b * a.H + h0 + hh, smax_local);
 }
 
-__global__ void set_lens_kernel(int32_t* lens, LensArg la, int B) {
-  int b = blockIdx.x * blockDim.x + threadIdx.x;
-  if (b < B) lens[b] = la.v[b];
+// lens[b] and every per-head copy head_lens[b][h] of the layer
+__global__ void set_lens_kernel(int32_t* lens, int32_t* head_lens, LensArg la, int B, int H) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < B * H) {
+    const int b = i / H;
+    head_lens[i] = la.v[b];
+    if (i % H == 0) lens[b] = la.v[b];
+  }
 }
 
 // ---------------------------------------------------------------- append ---
@@ -282,7 +287,7 @@ __global__ void set_lens_kernel(int32_t* lens, LensArg la, int B) {
 struct AppendArgs {
   QuantArgs k, v;       // x points at [B][H][D] new tokens (t_stride unused)
   int32_t* lens;        // device lens of the layer
-  uint32_t* tickets;    // [B]
+  int32_t* head_lens;   // [B][H] per-head length counters of the layer
   int warp_smem;        // per-warp scratch bytes for the per-token path
 };
 
@@ -298,9 +303,8 @@ __device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, 
   if (a.L.axis == 1) {
     const int G = a.L.group;
     const int slot = n & (G - 1);
-    __half* tail = tail_ptr(a, b, h);
-    for (int c = lane; c < D; c += 32)
-      tail[(long)slot * D + c] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
+    __half* tail = tail_ptr(a, b, h) + (long)slot * D;
+    for (int c = lane; c < D; c += 32) tail[c] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
     return slot == G - 1;
   }
   const int whole = a.L.whole;
@@ -331,6 +335,15 @@ __device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, 
   // merge into the tile words that hold token row trow
   const int trow = n & 15, tile = n >> 4;
   const Planes& pl = a.L.planes;
+  if (trow == 0) {
+    // a tile's first token clears the whole tile (a shorter re-prefill can leave
+    // older codes behind), so that later tokens only OR their bits in
+    for (int hh = 0; hh < nh; ++hh) {
+      uint4* dst = reinterpret_cast<uint4*>(codes_ptr(a, b, h + hh, tile));
+      for (int q = lane; q < a.L.tile_words / 4; q += 32) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+  }
   for (int hh = 0; hh < nh; ++hh) {
     uint32_t* dst = codes_ptr(a, b, h + hh, tile);
     const uint8_t* tc = cs + hh * D;
@@ -355,8 +368,10 @@ __device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, 
           }
         if (!m) continue;
         const int wi = D * off / 2 + ln * W + i;
-        const uint32_t old = trow == 0 ? 0u : dst[wi];  // a fresh tile starts from zero bits
-        dst[wi] = (old & ~m) | nv;
+        // the row's bits are zero (the tile was cleared at its first token), so
+        // the merge is a fire-and-forget OR with no read of the old word
+        if (trow == 0) dst[wi] = nv;
+        else atomicOr(dst + wi, nv);
       }
     }
   }
@@ -367,14 +382,19 @@ __device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, 
 
 // One CTA of 128 threads per (sequence, kv head): warp 0 appends the key, warp 1
 // the value; a per-channel tensor whose tail just filled up is then sealed by
-// all four warps.  The last CTA of a sequence advances its length (atomic
-// ticket, no waiting).
+// all four warps.  Each CTA reads and advances only its own per-head length
+// counter (no other CTA of the launch touches it), and the head-0 CTA also
+// advances the sequence length, which no CTA of the launch reads: no ticket,
+// fence or waiting is needed.
 __global__ void append_kernel(const __grid_constant__ AppendArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int seal[2];
   const int b = blockIdx.x, h = blockIdx.y;
   const int warp = threadIdx.x >> 5;
-  const int n = a.lens[b];
+  int32_t* my_len = a.head_lens + (long)b * gridDim.y + h;
+  pdl_wait();
+  pdl_trigger();  // the decode that follows may get its CTAs resident now
+  const int n = *my_len;
   const QuantArgs& t = warp == 0 ? a.k : a.v;
   if (threadIdx.x < 2) seal[threadIdx.x] = 0;
   __syncthreads();
@@ -404,13 +424,8 @@ __global__ void append_kernel(const __grid_constant__ AppendArgs a) {
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    __threadfence();
-    unsigned prev = atomicAdd(a.tickets + b, 1u);
-    if (prev == (unsigned)gridDim.y - 1u) {
-      a.lens[b] = n + 1;
-      a.tickets[b] = 0u;
-      __threadfence();
-    }
+    *my_len = n + 1;
+    if (h == 0) a.lens[b] = n + 1;
   }
 }
 
@@ -517,7 +532,8 @@ cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v
   LensArg la;
   for (int b = 0; b < B; ++b) la.v[b] = lens_host[b];
   int32_t* dl = C->d_lens + (long)layer * B;
-  set_lens_kernel<<<(B + 127) / 128, 128, 0, st>>>(dl, la, B);
+  int32_t* dhl = C->d_head_lens + (long)layer * B * H;
+  set_lens_kernel<<<(B * H + 127) / 128, 128, 0, st>>>(dl, dhl, la, B, H);
   ++*launches;
   // the layer's max-step statistics restart with the new contents
   for (int is_v = 0; is_v < 2; ++is_v) {
@@ -569,10 +585,13 @@ cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v,
   a.k = make_args(C, 0, layer, k, x_f32, 1);
   a.v = make_args(C, 1, layer, v, x_f32, 1);
   a.lens = C->d_lens + (long)layer * C->cfg.batch;
-  a.tickets = C->d_append_tickets;
+  a.head_lens = C->d_head_lens + (long)layer * C->cfg.batch * C->cfg.kv_heads;
   a.warp_smem = append_warp_smem(C);
   size_t sm = append_smem(C);
-  append_kernel<<<dim3(C->cfg.batch, C->cfg.kv_heads), 128, sm, st>>>(a);
+  void* args[] = {&a};
+  cudaError_t e = launch_pdl(reinterpret_cast<const void*>(&append_kernel), dim3(C->cfg.batch, C->cfg.kv_heads),
+                             dim3(128), sm, st, args);
+  if (e != cudaSuccess) return e;
   ++*launches;
   return cudaGetLastError();
 }
@@ -596,6 +615,7 @@ cudaError_t quant_setup(kvq_cache* C) {
     e = cudaFuncSetAttribute(prefill_token_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tok);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)append_smem(C));
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 

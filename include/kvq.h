@@ -211,11 +211,16 @@ kvq_status kvq_device_status(kvq_cache_t cache, void* stream);
  * step needs.  0 (default) plans for the current lengths. */
 kvq_status kvq_set_decode_plan(kvq_cache_t cache, int plan_tokens);
 
-/* Decode kernel choice: which = 0 (default) uses a compile-time specialisation
- * of the decode kernel when the cache's formats match one (fp16 metadata, no
- * whole-vector groups, formats of the benchmarked workloads), else the generic
- * kernel; which = 1 always uses the generic (runtime-format) kernel.  Both
- * compute the same result; the choice only affects speed. */
+/* Decode kernel choice, two bits.  Bit 0: 0 (default) uses a compile-time
+ * specialisation of the decode kernel when the cache's formats match one (fp16
+ * metadata, no whole-vector groups, formats of the benchmarked workloads), else
+ * the generic kernel; 1 always uses the generic (runtime-format) kernel.
+ * Bit 1: 0 (default) merges the split-K partials of a (sequence, kv head)
+ * inside one thread-block cluster when there are at most 8 splits (through
+ * distributed shared memory), else through the global workspace; 1 always uses
+ * the global workspace.  Every choice computes the same result (up to fp32
+ * summation order); they only affect speed.  which outside 0..3:
+ * KVQ_ERR_INVALID_ARG. */
 kvq_status kvq_set_decode_kernel(kvq_cache_t cache, int which);
 
 /* 1 if kvq_decode_attn currently runs a compile-time specialisation, else 0. */

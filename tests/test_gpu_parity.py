@@ -59,14 +59,16 @@ def decode_ref(wl, orq_k, orq_v, lens, q_cpu, scale):
     return oracle.attention(kh, vh, q_cpu.float().numpy(), np.array(lens, np.int32), scale)
 
 
-def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0, generic=None):
+def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0, generic=None, global_combine=False):
     """Prefill `lens` tokens of layer `layer`, compare the export and the decode output.
     generic: None keeps the default kernel choice, True forces the generic kernel,
-    False requires the compile-time specialisation."""
+    False requires the compile-time specialisation.  global_combine: merge the
+    split-K partials through the global workspace even when a cluster could."""
     T = max(max(lens), 1)
     cache = make_cache(wl, max_tokens=T, max_splits=max_splits, meta_dtype=kvq.F32 if meta_f32 else kvq.F16)
+    if generic is True or global_combine:
+        cache.kvq_set_decode_kernel((1 if generic else 0) | (2 if global_combine else 0))
     if generic is True:
-        cache.kvq_set_decode_kernel(1)
         assert not cache.kvq_decode_kernel_specialized()
     elif generic is False:
         assert cache.kvq_decode_kernel_specialized()
@@ -154,6 +156,18 @@ def test_specialized_and_generic_kernels(case, generic):
     name, B, Hq, H, D, kc, vc, lens = case
     wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=7)
     run_case(wl, lens, generic=generic)
+
+
+GLOBAL_COMBINE_CASES = [CASES[0], CASES[11], FAST_CASES[0], FAST_CASES[2], FAST_CASES[6]]
+
+
+@pytest.mark.parametrize("case", GLOBAL_COMBINE_CASES, ids=[c[0] for c in GLOBAL_COMBINE_CASES])
+def test_global_workspace_combine(case):
+    """The split-K partials merged through the global workspace and tickets
+    (the path for more than 8 splits) agree with the oracle at every size."""
+    name, B, Hq, H, D, kc, vc, lens = case
+    wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=8)
+    run_case(wl, lens, global_combine=True)
 
 
 @pytest.mark.parametrize("case", CASES[:6] + CASES[12:], ids=[c[0] for c in CASES[:6] + CASES[12:]])
