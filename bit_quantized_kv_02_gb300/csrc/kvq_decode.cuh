@@ -488,6 +488,14 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   const float2* cv_t1 = canV + (tk0 + 1) * gs_v;
   const float2* cv_t2 = canV + (tk0 + 8) * gs_v;
   const float2* cv_t3 = canV + (tk0 + 9) * gs_v;
+  // Per-token values with few groups per row (2 * rep * groups <= 8): every
+  // (query, value group, hi/lo) gets its own B column, so one B operand per
+  // tile carries all groups' step-scaled probabilities and each m-tile (one
+  // channel group) reads the columns of its group.  Lane column n = g:
+  // hi/lo = n & 1, group = (n >> 1) % groups, query = (n >> 1) / groups.
+  const bool GC = VAXIS == 0 && !R8 && 2 * rep * gs_v <= 8;
+  const int gc_grp = GC ? (g >> 1) % gs_v : 0;
+  const int pv_rho = GC ? (g >> 1) / gs_v : (g >> 1);
 
   // One 16-token tile.  FAST: the tile is full and both its keys and values are
   // packed (the bulk of every range), so the tail and partial-tile checks fold away.
@@ -660,7 +668,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
     }
     {
       // O columns of this thread: non-R8 (rho = tig, hi/lo), R8 (rho = 2tig, 2tig+1)
-      const float a0 = alpha[0], a1 = R8 ? alpha[1] : alpha[0];
+      float a0 = alpha[0], a1 = R8 ? alpha[1] : alpha[0];
+      if (GC) {  // this lane's O columns belong to query tig / groups
+        a0 = __shfl_sync(0xffffffffu, alpha[0], min(tig / gs_v, rep - 1));
+        a1 = a0;
+      }
       if (__any_sync(0xffffffffu, (a0 != 1.0f) || (a1 != 1.0f))) {
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
@@ -691,7 +703,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
       {
         const int srcA = 8 * tig, srcB = 8 * tig + 4;
         if (!R8) {
-          const int rho = g >> 1;
+          const int rho = pv_rho;
           pv[0] = __shfl_sync(0xffffffffu, p[0], srcA + rho);
           pv[1] = __shfl_sync(0xffffffffu, p[0], srcB + rho);
           pv[2] = __shfl_sync(0xffffffffu, p[1], srcA + rho);
@@ -756,9 +768,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
       };
       auto pv_packed = [&](auto vb) {
         constexpr int VB = decltype(vb)::value;
+        if (GC)
+          make_b(pv[0] * cv_t0[gc_grp].x, pv[1] * cv_t1[gc_grp].x, pv[2] * cv_t2[gc_grp].x, pv[3] * cv_t3[gc_grp].x);
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          if (VAXIS == 0 && (j & (cpgv - 1)) == 0) {
+          if (VAXIS == 0 && !GC && (j & (cpgv - 1)) == 0) {
             const int jg = j >> lg_cpgv;
             make_b(pv[0] * cv_t0[jg].x, pv[1] * cv_t1[jg].x, pv[2] * cv_t2[jg].x, pv[3] * cv_t3[jg].x);
           }
@@ -891,6 +905,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
   const int rowlen = D + 2;
   {
     const int lg_gsz = (VAXIS == 0 && !vwhole) ? v_lgG : 30;  // channel group of an output column
+    // groups-in-columns: this lane's columns belong to query tig / groups and
+    // value group tig % groups; the zero-point sums of that query come from
+    // the score-owner lanes of query rho (lane rho holds them after the reduction)
+    float zq[VAXIS == 0 ? GV_MAX : 1];
+    if (VAXIS == 0 && GC) {
+#pragma unroll
+      for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u)
+        zq[u] = __shfl_sync(0xffffffffu, Zs[u][0] + Zs[u][1], min(tig / gs_v, rep - 1));
+    }
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
 #pragma unroll
@@ -901,6 +924,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
         if (!R8) {
           v0 = O[j][2 * rr] + O[j][2 * rr + 1];
           rho0 = tig;
+          if (VAXIS == 0 && GC) rho0 = (tig % gs_v == (c >> lg_gsz)) ? tig / gs_v : -1;
           v1 = 0.0f;
           rho1 = -1;
         } else {
@@ -915,7 +939,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const
 #pragma unroll
           for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u)
             if (u == jg) {
-              z0 = R8 ? (Zs[u][0] + Zs[u][2]) : (Zs[u][0] + Zs[u][1]);
+              z0 = R8 ? (Zs[u][0] + Zs[u][2]) : (GC ? zq[u] : (Zs[u][0] + Zs[u][1]));
               z1 = R8 ? (Zs[u][1] + Zs[u][3]) : 0.0f;
             }
           v0 = v0 * inv_sc_v + z0;
