@@ -165,7 +165,9 @@ static cudaError_t plan_launch(kvq_cache* C, int layer, const void* q, int q_f32
   if (C->v.axis == 1) unit = std::max(unit, C->v.group);
   std::vector<int32_t> plan(C->lens.begin() + (long)layer * cfg.batch, C->lens.begin() + (long)(layer + 1) * cfg.batch);
   for (auto& x : plan) x = std::max(x, (int32_t)std::min(C->plan_tokens, C->cfg.max_tokens));
-  const int slots = C->sm_count * occ;
+  // about four resident CTAs (16 warps) per SM already keep the issue slots
+  // busy; planning for more only adds per-CTA fixed work
+  const int slots = C->sm_count * std::min(occ, 4);
   a.S = choose_split(C, plan.data(), unit, slots, C->max_chunks);
   a.Sw = a.S / kWarps;
   int maxn = 0;

@@ -267,10 +267,13 @@ struct StatCfg {
 // --------------------------------------------------------------- kernel ----
 
 // resident CTAs per SM the register budget is sized for
-__host__ __device__ constexpr int decode_min_blocks(int D) { return D == 64 ? 5 : (D == 128 ? 3 : 2); }
+// (compile-time configurations need fewer registers than the generic kernel)
+__host__ __device__ constexpr int decode_min_blocks(int D, bool is_static) {
+  return is_static ? (D == 64 ? 5 : (D == 128 ? 4 : 2)) : (D == 64 ? 5 : (D == 128 ? 3 : 2));
+}
 
 template <int D, bool R8, int VAXIS, class CFG>
-__global__ void __launch_bounds__(128, decode_min_blocks(D)) decode_kernel(const __grid_constant__ DecodeArgs a) {
+__global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages != 0)) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NCH = D / 16;                // 16-channel chunks / m-tiles
   constexpr int NB = R8 ? 2 : 1;             // B operands per chunk (hi/lo split over two MMAs)
