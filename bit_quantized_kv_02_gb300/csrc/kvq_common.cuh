@@ -37,10 +37,11 @@ constexpr int kCombineGroup = 16; // split-K partials merged per combine step
 constexpr int kMaxSplits = 1024;
 constexpr int kMaxCluster = 8;    // splits merged inside one thread-block cluster (portable size)
 
-// split-K workspace: chunk partials + group partials, and combine tickets
+// split-K workspace: chunk partials + group partials (rows of head_dim + 4
+// floats: outputs, m, l, two pad words), and combine tickets
 inline int combine_groups(int max_chunks) { return (max_chunks + kCombineGroup - 1) / kCombineGroup; }
 inline size_t decode_work_floats(long batch, long q_heads, int head_dim, int max_chunks) {
-  return (size_t)batch * q_heads * (max_chunks + combine_groups(max_chunks)) * (head_dim + 2);
+  return (size_t)batch * q_heads * (max_chunks + combine_groups(max_chunks)) * (head_dim + 4);
 }
 inline size_t decode_ticket_words(long batch, long kv_heads, int max_chunks) {
   return (size_t)batch * kv_heads * (1 + combine_groups(max_chunks));

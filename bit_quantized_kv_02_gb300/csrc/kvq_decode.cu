@@ -66,7 +66,7 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   a.max_chunks = C->max_chunks;
   a.work = C->d_work;
   a.max_groups = combine_groups(C->max_chunks);
-  a.gwork = C->d_work + (size_t)cfg.batch * cfg.q_heads * C->max_chunks * (D + 2);
+  a.gwork = C->d_work + (size_t)cfg.batch * cfg.q_heads * C->max_chunks * (D + 4);
   a.tickets = C->d_decode_tickets;
   a.err = C->d_err;
   const DecLayout L = dec_layout(D, rep, C->k.bits, C->k.axis, C->k.whole, C->k.gpt, C->k.meta_bytes, C->v.bits,
@@ -211,7 +211,7 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   if (e != cudaSuccess) return e;
   DecodeArgs& a = P.a;
   a.work = work;
-  a.gwork = work + (size_t)C->cfg.batch * C->cfg.q_heads * C->max_chunks * (C->cfg.head_dim + 2);
+  a.gwork = work + (size_t)C->cfg.batch * C->cfg.q_heads * C->max_chunks * (C->cfg.head_dim + 4);
   a.tickets = tickets;
   void* args[] = {&a};
   e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), C->dec_smem, st, args, a.csize);

@@ -970,6 +970,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   // CTA merge -> chunk partial in the workspace (cluster launch: in shared
   // memory after the four warp partials)
   float* part = mw + kWarps * rep * rowlen;
+  constexpr int wrow = D + 4;  // workspace row: D outputs, m, l, two pad (16-byte aligned rows)
   const long hqb = (long)b * H * rep + hq0;
   const int max_chunks = a.max_chunks;
   for (int i = threadIdx.x; i < rep * rowlen; i += blockDim.x) {
@@ -988,7 +989,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       }
     }
     if (a.csize) part[rho * rowlen + c] = acc;
-    else a.work[((hqb + rho) * max_chunks + chunk) * rowlen + c] = acc;
+    else a.work[((hqb + rho) * max_chunks + chunk) * wrow + c] = acc;
   }
   if (a.csize) {
     // Cluster merge: the splits of this (sequence, head) are the CTAs of one
@@ -1057,7 +1058,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     float* tot = sw + 2 * rep * K;   // [rep][2] (M, den)
     for (int i = threadIdx.x; i < rep * K; i += blockDim.x) {
       const int rho = i / K, k = i - rho * K;
-      const float* e = src0 + rho * qstride + (long)k * rowlen + D;
+      const float* e = src0 + rho * qstride + (long)k * wrow + D;
       wts[i] = __ldcg(e);
       lks[i] = __ldcg(e + 1);
     }
@@ -1076,24 +1077,37 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       tot[2 * rho + 1] = den;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
-      const int rho = i / D, c = i - rho * D;
-      const float* src = src0 + rho * qstride + c;
+    // four output columns per thread, up to kCombineGroup 16-byte loads in flight
+    for (int i4 = threadIdx.x; i4 < rep * D / 4; i4 += blockDim.x) {
+      const int rho = (4 * i4) / D, c = 4 * i4 - rho * D;
+      const float4* src = reinterpret_cast<const float4*>(src0 + rho * qstride + c);
       const float* w = wts + rho * K;
-      float num = 0.0f;
+      float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int k0 = 0; k0 < K; k0 += kCombineGroup) {
-        float v[kCombineGroup];
-#pragma unroll
-        for (int u = 0; u < kCombineGroup; ++u) v[u] = (k0 + u < K) ? __ldcg(src + (long)(k0 + u) * rowlen) : 0.0f;
+        float4 v[kCombineGroup];
 #pragma unroll
         for (int u = 0; u < kCombineGroup; ++u)
-          if (k0 + u < K) num += w[k0 + u] * v[u];
+          v[u] = (k0 + u < K) ? __ldcg(src + (long)(k0 + u) * (wrow / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kCombineGroup; ++u)
+          if (k0 + u < K) {
+            const float f = w[k0 + u];
+            num.x += f * v[u].x;
+            num.y += f * v[u].y;
+            num.z += f * v[u].z;
+            num.w += f * v[u].w;
+          }
       }
       if (final_out) {
         const float den = tot[2 * rho + 1];
-        a.out[(hqb + rho) * D + c] = den > 0.0f ? num / den : 0.0f;
+        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+        float* o = a.out + (hqb + rho) * D + c;
+        o[0] = num.x * inv;
+        o[1] = num.y * inv;
+        o[2] = num.z * inv;
+        o[3] = num.w * inv;
       } else {
-        dst0[rho * dst_qstride + c] = num;
+        *reinterpret_cast<float4*>(dst0 + rho * dst_qstride + c) = num;
       }
     }
     if (!final_out)
@@ -1102,14 +1116,14 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         dst0[rho * dst_qstride + D + 1] = tot[2 * rho + 1];
       }
   };
-  const float* part0 = a.work + (hqb * max_chunks + (long)grp * kCombineGroup) * rowlen;
+  const float* part0 = a.work + (hqb * max_chunks + (long)grp * kCombineGroup) * wrow;
   if (ngroups == 1) {
-    merge(part0, (long)max_chunks * rowlen, gsize, true, nullptr, 0);
+    merge(part0, (long)max_chunks * wrow, gsize, true, nullptr, 0);
     if (threadIdx.x == 0) tk[1 + grp] = 0u;
     return;
   }
-  float* g0 = a.gwork + (hqb * a.max_groups + grp) * rowlen;
-  merge(part0, (long)max_chunks * rowlen, gsize, false, g0, (long)a.max_groups * rowlen);
+  float* g0 = a.gwork + (hqb * a.max_groups + grp) * wrow;
+  merge(part0, (long)max_chunks * wrow, gsize, false, g0, (long)a.max_groups * wrow);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1119,7 +1133,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   __syncthreads();
   if (!last) return;
   __threadfence();
-  merge(a.gwork + hqb * a.max_groups * rowlen, (long)a.max_groups * rowlen, ngroups, true, nullptr, 0);
+  merge(a.gwork + hqb * a.max_groups * wrow, (long)a.max_groups * wrow, ngroups, true, nullptr, 0);
   if (threadIdx.x == 0) tk[0] = 0u;
 }
 

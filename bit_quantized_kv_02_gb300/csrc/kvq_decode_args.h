@@ -31,8 +31,8 @@ struct DecodeArgs {
   float scale_log2;         // softmax scale * log2(e)
   int S, Sw;                // tokens per CTA / per warp
   int max_chunks;
-  float* work;              // [B][H*rep][max_chunks][D+2] chunk partials
-  float* gwork;             // [B][H*rep][max_groups][D+2] group partials
+  float* work;              // [B][H*rep][max_chunks][D+4] chunk partials
+  float* gwork;             // [B][H*rep][max_groups][D+4] group partials
   int max_groups;           // ceil(max_chunks / kCombineGroup)
   int csize;                // > 0: the grid's x dimension forms clusters of csize CTAs (all splits of one
                             // sequence and head) that merge through distributed shared memory

@@ -18,7 +18,7 @@ struct kvq_cache {
   int32_t* d_head_lens = nullptr;       // [layers][batch][kv_heads] per-head copies of the lengths (append)
   uint32_t* d_decode_tickets = nullptr; // [batch][kv_heads]
   int* d_err = nullptr;                 // device error word
-  float* d_work = nullptr;              // split-K partials [batch][q_heads][max_chunks][head_dim + 2]
+  float* d_work = nullptr;              // split-K partials [batch][q_heads][max_chunks][head_dim + 4], then group partials
   int max_chunks = 0;
   std::vector<int32_t> lens;  // host mirror [layers][batch]
   int last_launches = 0;

@@ -161,7 +161,7 @@ kvq_status kvq_decode_attn(kvq_cache_t cache, int layer, const void* q, int q_dt
  * runtime whose device memory is laid out once by another component, or a
  * plugin that must not call cudaMalloc.  Allocates nothing.  The source pages
  * have no counterpart of this call; it is a deployment convenience.
- *  - Needs batch * q_heads * (max_splits + ceil(max_splits/16)) * (head_dim + 2)
+ *  - Needs batch * q_heads * (max_splits + ceil(max_splits/16)) * (head_dim + 4)
  *    * 4 bytes (rounded up to 256) + batch * kv_heads * (1 + ceil(max_splits/16))
  *    * 4 bytes <= 16 MiB, else KVQ_ERR_BUFFER_TOO_SMALL
  *    (nothing launched; kvq_last_error says how much was needed).

@@ -58,7 +58,7 @@ def test_static_scratch_matches_decode_twice(shape):
 
 
 def test_static_scratch_rejects_oversize():
-    # 64 sequences x 32 query heads x 1024 splits x 130 floats is far beyond the 16 MiB array
+    # 64 sequences x 32 query heads x 1024 splits x 132 floats is far beyond the 16 MiB array
     cfg = kvq.make_config(1, 64, 32, 8, 128, 4096, (2, 64, kvq.PER_CHANNEL, kvq.ASYM),
                           (2, 64, kvq.PER_TOKEN, kvq.ASYM), kvq.F16, 1024)
     cache = kvq.KVQCache(cfg)
