@@ -55,27 +55,62 @@ __host__ __device__ constexpr int pw_of(int b, int p) {
 }
 __host__ __device__ constexpr int po_of(int b, int p) { return p == 0 ? 0 : pw_of(b, 0) + (p == 2 ? pw_of(b, 1) : 0); }
 
-// Four fp16x2 MMA operand registers (pairs 4j..4j+3 of this lane) holding
-// 2^BITS + code, exact.
+// Code-to-operand conversion.  Widths 2, 4 and 8 place each code, unshifted
+// or after one shift shared by several registers, in the low mantissa bits of
+// an fp16 subnormal: the register's value is code * 2^(base - 24), exact, with
+// base = conv_r * (fragment row half) + conv_c * (fragment column half) (mma
+// takes subnormal fp16 operands exactly).  The other widths use an fp16 whose
+// exponent field makes its value 2^B + code (one rotate + one LOP3 per bit
+// plane).  Either way A = 2^(conv_g + base) * (code + conv_off).
+__host__ __device__ constexpr bool conv_subn(int b) { return b == 2 || b == 4 || b == 8; }
+__host__ __device__ constexpr int conv_g(int b) { return conv_subn(b) ? -24 : 0; }
+__host__ __device__ constexpr int conv_r(int b) { return b == 4 ? 4 : (b == 2 ? 2 : 0); }
+__host__ __device__ constexpr int conv_c(int b) { return b == 2 ? 4 : 0; }
+__host__ __device__ constexpr int conv_off(int b) { return conv_subn(b) ? 0 : (1 << b); }
+
+// Four fp16x2 MMA operand registers (pairs 4j..4j+3 of this lane, register r
+// = fragment row half + 2 * column half) of 16-channel chunk j.
 template <int BITS, int D>
 __device__ __forceinline__ void convert_chunk(const uint32_t* tile, int lane, int j, uint32_t a[4]) {
-  constexpr uint32_t magic = (uint32_t)((BITS + 15) << 10) * 0x00010001u;
+  if constexpr (BITS == 4) {
+    // one word per chunk and lane; pair r at bits 4r (+16)
+    const uint32_t w = tile[lane * (D / 16) + j], u = w >> 8;
+    a[0] = w & 0x000F000Fu;
+    a[1] = w & 0x00F000F0u;
+    a[2] = u & 0x000F000Fu;
+    a[3] = u & 0x00F000F0u;
+  } else if constexpr (BITS == 2) {
+    // one word per two chunks; pair 4(j & 1) + r at bits 2(4(j & 1) + r) (+16)
+    const uint32_t w0 = tile[lane * (D / 32) + (j >> 1)];
+    const uint32_t w = (j & 1) ? (w0 >> 8) : w0;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) a[r] = magic;
+    for (int r = 0; r < 4; ++r) a[r] = w & (0x00030003u << (2 * r));
+  } else if constexpr (BITS == 8) {
+    // two words per chunk; pair r at bytes (r & 1) and 2 + (r & 1) of word r / 2
+    const uint32_t w0 = tile[lane * (D / 8) + 2 * j], w1 = tile[lane * (D / 8) + 2 * j + 1];
+    a[0] = __byte_perm(w0, 0u, 0x4240);
+    a[1] = __byte_perm(w0, 0u, 0x4341);
+    a[2] = __byte_perm(w1, 0u, 0x4240);
+    a[3] = __byte_perm(w1, 0u, 0x4341);
+  } else {
+    constexpr uint32_t magic = (uint32_t)((BITS + 15) << 10) * 0x00010001u;
 #pragma unroll
-  for (int p = 0; p < np_of(BITS); ++p) {
-    const int w = pw_of(BITS, p), off = po_of(BITS, p);
-    const int W = D * w / 64, P = 16 / w;
-    const int pos = 10 - BITS + off;
-    const uint32_t M = (((1u << w) - 1u) << pos) * 0x00010001u;
-    const uint32_t* pl = tile + D * off / 2 + lane * W;
+    for (int r = 0; r < 4; ++r) a[r] = magic;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int pi = 4 * j + r;
-      const uint32_t word = pl[pi / P];
-      const int k = pi % P;
-      const int sh = (pos - k * w) & 31;
-      a[r] = lop3_and_or(sh ? rotl(word, sh) : word, M, a[r]);
+    for (int p = 0; p < np_of(BITS); ++p) {
+      const int w = pw_of(BITS, p), off = po_of(BITS, p);
+      const int W = D * w / 64, P = 16 / w;
+      const int pos = 10 - BITS + off;
+      const uint32_t M = (((1u << w) - 1u) << pos) * 0x00010001u;
+      const uint32_t* pl = tile + D * off / 2 + lane * W;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int pi = 4 * j + r;
+        const uint32_t word = pl[pi / P];
+        const int k = pi % P;
+        const int sh = (pos - k * w) & 31;
+        a[r] = lop3_and_or(sh ? rotl(word, sh) : word, M, a[r]);
+      }
     }
   }
 }
@@ -93,18 +128,22 @@ __device__ __forceinline__ void convert_dispatch(int bits, const uint32_t* tile,
   }
 }
 
-// Stored metadata entries [0, n) -> fp32 (step * post_scale, zero') with
-// zero' = zero - 2^B step (symmetric: zero = -2^(B-1) step), so that a value is
-// step * (2^B + code) + zero'.  One warp, entries strided over the lanes.
-__device__ __forceinline__ void canon_meta(const char* src, int n, int bits, int sym, int meta_f32, float post_scale,
-                                           float2* dst, int lane) {
-  const float off = (float)(1 << bits);
-  const float soff = 0.5f * off;
+// Stored metadata entries [0, n) -> fp32 (step * post, zero') with zero' =
+// zero - conv_off * step (symmetric: zero = -2^(B-1) step), so that a value is
+// step * (code + conv_off) + zero'.  post = post_hi for the entries of the
+// upper fragment half (hsel > 0: entries i >= hsel, i.e. tokens 8..15 of a
+// per-token tile; hsel <= 0: channels with bit 3 set), else post_lo.  One
+// warp, entries strided over the lanes.
+__device__ __forceinline__ void canon_meta(const char* src, int n, int bits, int sym, int meta_f32, float post_lo,
+                                           float post_hi, int hsel, float2* dst, int lane) {
+  const float off = (float)conv_off(bits);
+  const float soff = (float)(1 << (bits - 1));
   for (int i = lane; i < n; i += 32) {
     float z, s;
     load_meta(src, i, meta_f32, sym, &z, &s);
     if (sym) z = -s * soff;
-    dst[i] = make_float2(s * post_scale, z - off * s);
+    const bool hi = hsel > 0 ? (i >= hsel) : ((i & 8) != 0);
+    dst[i] = make_float2(s * (hi ? post_hi : post_lo), z - off * s);
   }
 }
 
@@ -119,11 +158,13 @@ struct Slots {
 
 // Fragment-ordered QK B operand of one warp: q * s_c (kc = canonical
 // per-channel key metadata of the current group) or q (kc == null), scaled by
-// 2^E (E returned) and split into fp16 hi + lo; bias[rho] = sum_c q_c zero'_c.
-// Only valid query columns are written; the rest of barea stays zero.
+// 2^E, channels of the upper half of each 16-channel chunk further by chi (the
+// conversion's column scale), and split into fp16 hi + lo; bias[rho] =
+// sum_c q_c zero'_c.  Only valid query columns are written; the rest of barea
+// stays zero.
 template <int D, bool R8>
 __device__ __forceinline__ void build_qb(const float* qs, int rep, const float2* kc, uint32_t* barea, float* bias,
-                                         int E, int lane) {
+                                         int E, float chi, int lane) {
   const float sc = exp2i(E);
   for (int rho = 0; rho < rep; ++rho) {
     float bacc = 0.0f;
@@ -131,11 +172,12 @@ __device__ __forceinline__ void build_qb(const float* qs, int rep, const float2*
     for (int it = 0; it < D / 64; ++it) {
       const int c = 2 * (lane + 32 * it);
       const float2 q2 = *reinterpret_cast<const float2*>(qs + rho * D + c);
-      float s0 = sc, s1 = sc;
+      const float scc = (c & 8) ? sc * chi : sc;
+      float s0 = scc, s1 = scc;
       if (kc) {
         const float4 m = *reinterpret_cast<const float4*>(kc + c);
-        s0 = m.x * sc;
-        s1 = m.z * sc;
+        s0 = m.x * scc;
+        s1 = m.z * scc;
         bacc += q2.x * m.y + q2.y * m.w;
       }
       const float v0 = q2.x * s0, v1 = q2.y * s1;
@@ -468,8 +510,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int E_chan = k_token ? E_unit : norm_exp(qmax * smax_k);
   int Ek = E_unit;
   bool qb_unit = false;
+  // conversion exponents of the key and value codes (A = 2^(g + r*rowhalf +
+  // c*colhalf) * (code + off)): key columns are channels (compensated in the
+  // query operand), key rows tokens (in the score fold); value rows are
+  // channels (at the output), value columns tokens (in the P operand)
+  const int k_cg = conv_g(kbits), k_cr = conv_r(kbits);
+  const float k_chi = exp2i(-conv_c(kbits));
+  const int v_cg = conv_g(vbits), v_cr = conv_r(vbits);
+  const float v_chi = exp2i(-conv_c(vbits));
   if (k_token) {
-    build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, lane);
+    build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, k_chi, lane);
     qb_unit = true;
     load_b();
   }
@@ -518,26 +568,30 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     // ---- metadata of this stage -> canonical fp32 pairs
     if (kp) {
       if (k_token) {
-        canon_meta(reinterpret_cast<const char*>(st + st_km), kTile * gs_k, kbits, ksym, kf32, exp2i(-Ek), canK, lane);
+        canon_meta(reinterpret_cast<const char*>(st + st_km), kTile * gs_k, kbits, ksym, kf32, exp2i(-Ek - k_cg),
+                   exp2i(-Ek - k_cg - k_cr), 8 * gs_k, canK, lane);
       } else if ((t0 & kgmask) == 0) {
-        canon_meta(reinterpret_cast<const char*>(st + st_km), D, kbits, ksym, kf32, 1.0f, canK, lane);
+        canon_meta(reinterpret_cast<const char*>(st + st_km), D, kbits, ksym, kf32, 1.0f, 1.0f, 0, canK, lane);
         __syncwarp();
         Ek = E_chan;
-        build_qb<D, R8>(qs, rep, canK, barea, wbias, E_chan, lane);
+        build_qb<D, R8>(qs, rep, canK, barea, wbias, E_chan, k_chi, lane);
         qb_unit = false;
         load_b();
       }
     } else if (!qb_unit) {
+      // fp16 tail of per-channel keys: plain operands, no conversion scale
       Ek = E_unit;
-      build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, lane);
+      build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, 1.0f, lane);
       qb_unit = true;
       load_b();
     }
     if (vp) {
       if (VAXIS == 0)
-        canon_meta(reinterpret_cast<const char*>(st + st_vm), kTile * gs_v, vbits, vsym, vf32, sc_v, canV, lane);
+        canon_meta(reinterpret_cast<const char*>(st + st_vm), kTile * gs_v, vbits, vsym, vf32, sc_v, sc_v * v_chi,
+                   8 * gs_v, canV, lane);
       else if (vflush)
-        canon_meta(reinterpret_cast<const char*>(st + st_vm), D, vbits, vsym, vf32, 1.0f, canV, lane);
+        canon_meta(reinterpret_cast<const char*>(st + st_vm), D, vbits, vsym, vf32, exp2i(-v_cg), exp2i(-v_cg - v_cr), 0,
+                   canV, lane);
     }
     __syncwarp();
 
@@ -550,7 +604,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       float C2[4] = {0.f, 0.f, 0.f, 0.f};  // second accumulation chain (odd chunks)
       const uint32_t* ktile = reinterpret_cast<const uint32_t*>(st + st_kc);
       const bool ktok = kp && k_token;
-      const float inv_e = exp2i(-Ek);
+      // packed keys: undo 2^Ek and the conversion's row exponent
+      const float inv_e0 = exp2i(-Ek - (kp ? k_cg : 0)), inv_e1 = exp2i(-Ek - (kp ? k_cg + k_cr : 0));
       auto fold = [&](int jg) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) C[r] += C2[r];
@@ -562,9 +617,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
             const int rho = min(SL::rho(q, tig), rep - 1);
             score[q] += m.x * v + m.y * qg[jg * rep + rho];
           } else if (kp) {
-            score[q] += v * inv_e + wbias[SL::rho(q, tig)];
+            score[q] += v * (SL::rh(q) ? inv_e1 : inv_e0) + wbias[SL::rho(q, tig)];
           } else {
-            score[q] += v * inv_e;
+            score[q] += v * inv_e0;
           }
         }
 #pragma unroll
@@ -785,7 +840,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         }
       };
       if (vp) {
-        if (VAXIS == 1) make_b(pv[0], pv[1], pv[2], pv[3]);
+        if (VAXIS == 1) make_b(pv[0], pv[1], pv[2] * v_chi, pv[3] * v_chi);
         switch (vbits) {
           case 2: pv_packed(IntC<2>{}); break;
           case 3: pv_packed(IntC<3>{}); break;
@@ -945,8 +1000,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
               z0 = R8 ? (Zs[u][0] + Zs[u][2]) : (GC ? zq[u] : (Zs[u][0] + Zs[u][1]));
               z1 = R8 ? (Zs[u][1] + Zs[u][3]) : 0.0f;
             }
-          v0 = v0 * inv_sc_v + z0;
-          v1 = v1 * inv_sc_v + z1;
+          const float osc = inv_sc_v * exp2i(-v_cg - (rr ? v_cr : 0));  // 2^-E_v and the conversion's row exponent
+          v0 = v0 * osc + z0;
+          v1 = v1 * osc + z1;
         }
         if (rho0 >= 0 && rho0 < rep) mw[(warp * rep + rho0) * rowlen + c] = v0;
         if (rho1 >= 0 && rho1 < rep) mw[(warp * rep + rho1) * rowlen + c] = v1;
