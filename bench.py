@@ -87,8 +87,9 @@ def decode_source_hash() -> str:
 
 
 def ncu_traffic(workload_name: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on the current decode kernel source (else None)."""
+    """DRAM bytes per decode launch from the committed ncu summary of this
+    workload (profiles/decode_kernel_<--workload>.md), if it was taken on the
+    current decode kernel source (else None)."""
     p = os.path.join(ROOT, "profiles", f"decode_kernel_{workload_name}.md")
     if not os.path.exists(p):
         return None
@@ -362,7 +363,7 @@ def run_ours(args, rank, world):
                        "l2": "256 MB buffer written before every timed step (L2 flushed)",
                        "parallelism": f"dp{world} (sequences sharded, no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(wl.name),
+                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload) if not args.tokens else None,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback",
                          "kernel": "decode_kernel", "bytes_per_launch": round(dec_bytes_per_launch),

@@ -60,7 +60,7 @@ typedef enum {
   KVQ_ERR_CAPACITY = 3,       /* a sequence would exceed max_tokens */
   KVQ_ERR_BUFFER_TOO_SMALL = 4, /* device buffer smaller than kvq_bytes.alloc */
   KVQ_ERR_CUDA = 5,           /* a CUDA runtime error (launch or asynchronous) */
-  KVQ_ERR_DEVICE_TIMEOUT = 6  /* a bounded device-side wait gave up */
+  KVQ_ERR_DEVICE_TIMEOUT = 6  /* a device-side wait gave up (reserved: no kernel waits today) */
 } kvq_status;
 
 typedef enum { KVQ_PER_TOKEN = 0, KVQ_PER_CHANNEL = 1 } kvq_axis; /* group along channels / along tokens */
@@ -198,14 +198,15 @@ kvq_status kvq_get_lens(kvq_cache_t cache, int layer, int32_t* lens_host);
  * element), the algorithmic traffic of the path.  Host only. */
 kvq_status kvq_decode_traffic(kvq_cache_t cache, int layer, int q_dtype, double* bytes);
 
-/* Synchronise `stream` and report whether a bounded device-side wait of an
- * earlier kernel on this handle gave up (KVQ_ERR_DEVICE_TIMEOUT; the flag is
- * then cleared) or a CUDA error is pending (KVQ_ERR_CUDA). */
+/* Synchronise `stream` and report whether a kernel on this handle recorded a
+ * device-side failure in the handle's error word (KVQ_ERR_DEVICE_TIMEOUT; the
+ * word is then cleared; the current kernels contain no device-side wait that
+ * could set it) or a CUDA error is pending (KVQ_ERR_CUDA). */
 kvq_status kvq_device_status(kvq_cache_t cache, void* stream);
 
 /* Decode split plan hint: when plan_tokens > 0, kvq_decode_attn sizes its
  * split-K launch as if every sequence held max(its length, plan_tokens) tokens
- * (CTAs past a sequence's real length exit at once).  A launch planned this way
+ * (CTAs past a sequence's real length do no work).  A launch planned this way
  * stays valid while the cache grows up to plan_tokens, which is what a CUDA
  * graph that captured kvq_append + kvq_decode_attn and is replayed step after
  * step needs.  0 (default) plans for the current lengths. */
