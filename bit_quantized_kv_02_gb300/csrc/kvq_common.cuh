@@ -193,23 +193,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// 16-byte asynchronous global -> shared copy that bypasses L1; completion is
-// tracked per thread in commit groups (cp.async.commit_group / wait_group).
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem_dst)), "l"(gsrc) : "memory");
+// 16-byte asynchronous global -> shared copy that bypasses L1 (shared-window
+// address); completion is tracked per thread in commit groups
+// (cp.async.commit_group / wait_group).  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async16_s(uint32_t smem_dst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_dst), "l"(gsrc) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
-// bytes (a multiple of 16, both addresses 16-byte aligned) copied by the 32
-// lanes of a warp, 16 bytes per lane and step
-__device__ __forceinline__ void warp_copy(void* dst, const void* src, int bytes, int lane) {
-  for (int o = lane * 16; o < bytes; o += 512)
-    cp_async16(static_cast<char*>(dst) + o, static_cast<const char*>(src) + o);
-}
-
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while the previous kernel of the stream still runs;
 // pdl_wait() returns once that kernel has completed and its writes are

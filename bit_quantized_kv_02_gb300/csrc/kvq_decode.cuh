@@ -156,16 +156,52 @@ struct Slots {
 
 // -------------------------------------------------- query operand build ---
 
-// Fragment-ordered QK B operand of one warp: q * s_c (kc = canonical
-// per-channel key metadata of the current group) or q (kc == null), scaled by
-// 2^E, channels of the upper half of each 16-channel chunk further by chi (the
-// conversion's column scale), and split into fp16 hi + lo; bias[rho] =
-// sum_c q_c zero'_c.  Only valid query columns are written; the rest of barea
-// stays zero.
+// Stored (zero, step) of entries c and c+1 (c even) in one vector load.
+__device__ __forceinline__ void load_meta2(const char* meta, int c, int meta_f32, int sym, float* z0, float* s0,
+                                           float* z1, float* s1) {
+  if (!meta_f32) {
+    if (sym) {
+      const __half2 v = *reinterpret_cast<const __half2*>(meta + 2 * c);
+      *s0 = __low2float(v);
+      *s1 = __high2float(v);
+      *z0 = *z1 = 0.0f;
+    } else {
+      const uint2 v = *reinterpret_cast<const uint2*>(meta + 4 * c);
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&v.x));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&v.y));
+      *z0 = a.x;
+      *s0 = a.y;
+      *z1 = b.x;
+      *s1 = b.y;
+    }
+  } else {
+    if (sym) {
+      const float2 v = *reinterpret_cast<const float2*>(meta + 4 * c);
+      *s0 = v.x;
+      *s1 = v.y;
+      *z0 = *z1 = 0.0f;
+    } else {
+      const float4 v = *reinterpret_cast<const float4*>(meta + 8 * c);
+      *z0 = v.x;
+      *s0 = v.y;
+      *z1 = v.z;
+      *s1 = v.w;
+    }
+  }
+}
+
+// Fragment-ordered QK B operand of one warp: q * s_c (kmeta = the stored
+// per-channel key metadata of the current group, read straight from the
+// stage) or q (kmeta == null), scaled by 2^E, channels of the upper half of
+// each 16-channel chunk further by chi (the conversion's column scale), and
+// split into fp16 hi + lo; bias[rho] = sum_c q_c zero'_c with zero' = zero -
+// conv_off * step (symmetric zero = -2^(B-1) step).  Only valid query columns
+// are written; the rest of barea stays zero.
 template <int D, bool R8>
-__device__ __forceinline__ void build_qb(const float* qs, int rep, const float2* kc, uint32_t* barea, float* bias,
-                                         int E, float chi, int lane) {
+__device__ __forceinline__ void build_qb(const float* qs, int rep, const char* kmeta, int kbits, int ksym, int kf32,
+                                         uint32_t* barea, float* bias, int E, float chi, int lane) {
   const float sc = exp2i(E);
+  const float koff = (float)conv_off(kbits), ksoff = (float)(1 << (kbits - 1));
   for (int rho = 0; rho < rep; ++rho) {
     float bacc = 0.0f;
 #pragma unroll
@@ -174,11 +210,16 @@ __device__ __forceinline__ void build_qb(const float* qs, int rep, const float2*
       const float2 q2 = *reinterpret_cast<const float2*>(qs + rho * D + c);
       const float scc = (c & 8) ? sc * chi : sc;
       float s0 = scc, s1 = scc;
-      if (kc) {
-        const float4 m = *reinterpret_cast<const float4*>(kc + c);
-        s0 = m.x * scc;
-        s1 = m.z * scc;
-        bacc += q2.x * m.y + q2.y * m.w;
+      if (kmeta) {
+        float z0, st0, z1, st1;
+        load_meta2(kmeta, c, kf32, ksym, &z0, &st0, &z1, &st1);
+        if (ksym) {
+          z0 = -st0 * ksoff;
+          z1 = -st1 * ksoff;
+        }
+        s0 = st0 * scc;
+        s1 = st1 * scc;
+        bacc += q2.x * (z0 - koff * st0) + q2.y * (z1 - koff * st1);
       }
       const float v0 = q2.x * s0, v1 = q2.y * s1;
       const __half2 hh = __floats2half2_rn(v0, v1);
@@ -193,7 +234,7 @@ __device__ __forceinline__ void build_qb(const float* qs, int rep, const float2*
         barea[((2 * j + 1) * 32 + 4 * rho + ttig) * 2 + breg] = *reinterpret_cast<const uint32_t*>(&ll);
       }
     }
-    if (kc) {
+    if (kmeta) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) bacc += __shfl_xor_sync(0xffffffffu, bacc, o);
       if (lane == 0) bias[rho] = bacc;
@@ -397,39 +438,36 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int kgmask = k_token ? 0 : kG - 1;
   const int vgmask = VAXIS == 0 ? 0 : vG - 1;
 
-  // stage i of this warp's range: every lane copies its 16-byte pieces
+  // Stage i of this warp's range: every lane copies its 16-byte pieces.  Tiles
+  // are issued in order, so the sources are running pointers (already offset
+  // by the lane) and only the shared-memory slot depends on i.
+  const uint32_t st_lane = smem_u32(stages) + lane * 16;
+  const char* kc_g = kc_src + lane * 16;
+  const char* vc_g = vc_src + lane * 16;
+  const char* km_g = km_src + lane * 16;
+  const char* vm_g = vm_src + lane * 16;
+  auto lane_copy = [&](uint32_t sdst, const char* gsrc, int bytes) {
+    for (int o = 0; o < bytes - lane * 16; o += 512) cp_async16_s(sdst + o, gsrc + o);
+  };
   auto issue = [&](int i) {
-    const int s = i & (ns - 1);
     const int t0 = w0 + i * kTile;
-    unsigned char* st = stages + s * stage_bytes;
-    const bool kp = t0 < sealed_k, vp = t0 < sealed_v;
-    uint32_t bytes = 0, kmb_i = 0, vmb_i = 0;
-    const char* kms = km_src;
-    const char* vms = vm_src;
-    if (kp) {
-      if (k_token) {
-        kms += (long)i * km_bytes;
-        kmb_i = km_bytes;
-      } else if ((t0 & kgmask) == 0) {
-        kms += (long)((t0 - w0) >> k_lgG) * km_bytes;
-        kmb_i = km_bytes;
+    const uint32_t sa = st_lane + (i & (ns - 1)) * stage_bytes;
+    if (t0 < sealed_k) {
+      lane_copy(sa + st_kc, kc_g, kc_bytes);
+      if (k_token || (t0 & kgmask) == 0) {  // per-token: every tile; per-channel: at a group's first tile
+        lane_copy(sa + st_km, km_g, km_bytes);
+        km_g += km_bytes;
       }
-      bytes += kc_bytes + kmb_i;
     }
-    if (vp) {
-      if (VAXIS == 0) {
-        vms += (long)i * vm_bytes;
-        vmb_i = vm_bytes;
-      } else if (((t0 + kTile) & vgmask) == 0) {
-        vms += (long)((t0 - w0) >> v_lgG) * vm_bytes;
-        vmb_i = vm_bytes;
+    kc_g += kc_bytes;
+    if (t0 < sealed_v) {
+      lane_copy(sa + st_vc, vc_g, vc_bytes);
+      if (VAXIS == 0 || ((t0 + kTile) & vgmask) == 0) {  // per-channel: at a group's last tile
+        lane_copy(sa + st_vm, vm_g, vm_bytes);
+        vm_g += vm_bytes;
       }
-      bytes += vc_bytes + vmb_i;
     }
-    if (kp) warp_copy(st + st_kc, kc_src + (long)i * kc_bytes, kc_bytes, lane);
-    if (kmb_i) warp_copy(st + st_km, kms, kmb_i, lane);
-    if (vp) warp_copy(st + st_vc, vc_src + (long)i * vc_bytes, vc_bytes, lane);
-    if (vmb_i) warp_copy(st + st_vm, vms, vmb_i, lane);
+    vc_g += vc_bytes;
   };
 
   // the first stages go out before the query set-up, so their DRAM latency
@@ -519,7 +557,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int v_cg = conv_g(vbits), v_cr = conv_r(vbits);
   const float v_chi = exp2i(-conv_c(vbits));
   if (k_token) {
-    build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, k_chi, lane);
+    build_qb<D, R8>(qs, rep, nullptr, kbits, ksym, kf32, barea, wbias, E_unit, k_chi, lane);
     qb_unit = true;
     load_b();
   }
@@ -571,17 +609,16 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         canon_meta(reinterpret_cast<const char*>(st + st_km), kTile * gs_k, kbits, ksym, kf32, exp2i(-Ek - k_cg),
                    exp2i(-Ek - k_cg - k_cr), 8 * gs_k, canK, lane);
       } else if ((t0 & kgmask) == 0) {
-        canon_meta(reinterpret_cast<const char*>(st + st_km), D, kbits, ksym, kf32, 1.0f, 1.0f, 0, canK, lane);
-        __syncwarp();
         Ek = E_chan;
-        build_qb<D, R8>(qs, rep, canK, barea, wbias, E_chan, k_chi, lane);
+        build_qb<D, R8>(qs, rep, reinterpret_cast<const char*>(st + st_km), kbits, ksym, kf32, barea, wbias, E_chan,
+                        k_chi, lane);
         qb_unit = false;
         load_b();
       }
     } else if (!qb_unit) {
       // fp16 tail of per-channel keys: plain operands, no conversion scale
       Ek = E_unit;
-      build_qb<D, R8>(qs, rep, nullptr, barea, wbias, E_unit, 1.0f, lane);
+      build_qb<D, R8>(qs, rep, nullptr, kbits, ksym, kf32, barea, wbias, E_unit, 1.0f, lane);
       qb_unit = true;
       load_b();
     }

@@ -44,7 +44,7 @@ struct DecodeArgs {
   int st_kc, st_km, st_vc, st_vm;  // offsets inside a stage
   int warp_bytes;           // per-warp region: B operand + canonical metadata + stages
   int barea_bytes;
-  int canon_k, canon_v;     // canonical (step, zero') entries per warp for keys / values
+  int canon_k, canon_v;     // canonical (step, zero') entries per warp for per-token keys / values
   int stage_off;            // offset of the stage ring inside the per-warp region
   int head_bytes;           // CTA head region (q, group sums)
 };
@@ -75,7 +75,7 @@ __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, in
   L.stage_bytes = dl_round(L.st_vm + L.vm_bytes, 128);
   L.lg_ns = L.stage_bytes <= 4096 ? 2 : 1;
   L.barea_bytes = (D / 16) * 32 * 8 * (rep == 8 ? 2 : 1);
-  L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : D;
+  L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : 0;  // per-channel keys are read from the stage
   L.canon_v = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) : D;
   L.stage_off = dl_round(L.barea_bytes + (L.canon_k + L.canon_v) * 8 + 32, 128);
   L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns), 128);
