@@ -326,6 +326,37 @@ def run_ours(args, rank, world):
     clk = clocks.stop() if clocks else None
     clocks = None
     kdist.barrier()
+    # materialised baseline (optional): per layer kvq_dequantize into fp16 rows,
+    # then decode attention over those rows; timed like the fused decode graph
+    mat = None
+    if args.materialized:
+        shape = (B, H, cap, D)
+        k16 = torch.zeros(shape, dtype=torch.float16, device=dev)
+        v16 = torch.zeros(shape, dtype=torch.float16, device=dev)
+        out_m = torch.empty_like(out)
+        graph_mat = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_mat, stream=stream):
+            for l in range(L):
+                cache.kvq_dequantize(l, k16, v16, stream=stream)
+                cache.kvq_decode_attn_materialized(l, k16, v16, qin[l], out_m[l], scale, stream=stream)
+        t_mat = []
+        for r in range(warm + steps):
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                e0.record(stream)
+                graph_mat.replay()
+                e1.record(stream)
+            stream.synchronize()
+            if r >= warm:
+                t_mat.append(e0.elapsed_time(e1))
+        fused_ms = t_decode / steps
+        mat_ms = float(np.mean(t_mat))
+        diff = (out_m - out).abs().max().item() / max(out.abs().max().item(), 1e-30)
+        mat = {"ms_per_step": round(mat_ms, 4), "fused_decode_ms_per_step": round(fused_ms, 4),
+               "fused_speedup": round(mat_ms / fused_ms, 2), "max_rel_diff_vs_fused": diff,
+               "path": "per layer: kvq_dequantize (packed -> fp16 rows) + kvq_decode_attn_materialized",
+               "fp16_bytes_written_and_read_per_layer": 2 * 2 * sum(wl.lens) * H * D * 2}
+        del k16, v16
     # end-to-end: host inputs -> device -> host outputs, same graph
     t_e2e = 0.0
     for s in range(e2e_steps):
@@ -377,6 +408,8 @@ def run_ours(args, rank, world):
                     "path": "pinned host -> device copies, graph of kvq_append + kvq_decode_attn, device -> host"},
             "clocks": clk,
         }
+        if mat is not None:
+            res["materialized"] = mat
     return res, wl
 
 
@@ -423,6 +456,8 @@ def main():
     ap.add_argument("--workload", default="gpt2_small")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--tokens", type=int, default=0, help="cap the cached tokens per sequence (profiling runs)")
+    ap.add_argument("--materialized", action="store_true",
+                    help="also time the materialised baseline (dequantize to fp16, then decode) beside the fused path")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

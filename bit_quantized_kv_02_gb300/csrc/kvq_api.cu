@@ -293,6 +293,28 @@ kvq_status kvq_decode_attn(kvq_cache_t C, int layer, const void* q, int q_dtype,
   return cuda_status(C, e);
 }
 
+kvq_status kvq_dequantize(kvq_cache_t C, int layer, void* k_out, void* v_out, void* stream) {
+  kvq_status s = layer_ok(C, layer);
+  if (s != KVQ_OK) return s;
+  if (!k_out || !v_out) return KVQ_ERR_INVALID_ARG;
+  C->last_launches = 0;
+  cudaError_t e = launch_dequantize(C, layer, k_out, v_out, static_cast<cudaStream_t>(stream), &C->last_launches);
+  return cuda_status(C, e);
+}
+
+kvq_status kvq_decode_attn_materialized(kvq_cache_t C, int layer, const void* k16, const void* v16, const void* q,
+                                        int q_dtype, float softmax_scale, float* out, void* stream) {
+  kvq_status s = layer_ok(C, layer);
+  if (s != KVQ_OK) return s;
+  if (!k16 || !v16 || !q || !out || (q_dtype != KVQ_F16 && q_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f)) softmax_scale = 1.0f / std::sqrt((float)C->cfg.head_dim);
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  C->last_launches = 0;
+  cudaError_t e = launch_decode_materialized(C, layer, k16, v16, q, q_dtype == KVQ_F32, softmax_scale, out,
+                                             static_cast<cudaStream_t>(stream), &C->last_launches);
+  return cuda_status(C, e);
+}
+
 kvq_status kvq_export(kvq_cache_t C, int layer, uint8_t* codes_k, uint8_t* codes_v, float* meta_k, float* meta_v,
                       uint16_t* tail_k, uint16_t* tail_v, int32_t* lens, void* stream) {
   kvq_status s = layer_ok(C, layer);

@@ -219,4 +219,68 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   return e;
 }
 
+// Decode over fp16 K / V rows materialised by kvq_dequantize ([B][Hkv][max_tokens][D]):
+// the same kernel (runtime formats, per-channel axis for both tensors) with
+// every token in its fp16 tail path, i.e. no packed tiles and no metadata.
+cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16, const void* v16, const void* q,
+                                       int q_f32, float scale, float* out, cudaStream_t st, int* launches) {
+  const kvq_config& cfg = C->cfg;
+  const int D = cfg.head_dim, rep = cfg.q_heads / cfg.kv_heads;
+  void* fn = pick_kernel(D, rep == 8, 1);
+  if (!fn) return cudaErrorInvalidValue;
+  Plan P;
+  int occ_unused = 1;
+  cudaError_t e = make_plan(C, layer, &P, &occ_unused);
+  if (e != cudaSuccess) return e;
+  DecodeArgs& a = P.a;
+  auto tail_only = [&](DecTensor& d, const void* rows) {
+    d.tail = static_cast<const __half*>(rows);
+    d.axis = 1;
+    d.whole = 0;
+    d.group = cfg.max_tokens;  // row stride of a (sequence, head)
+    d.lg_group = 30;           // nothing is ever sealed
+    d.gpt = 0;
+  };
+  tail_only(a.K, k16);
+  tail_only(a.V, v16);
+  const DecLayout L = dec_layout(D, rep, a.K.bits, 1, 0, 0, a.K.meta_bytes, a.V.bits, 1, 0, 0, a.V.meta_bytes);
+  a.st_kc = L.st_kc;
+  a.st_km = L.st_km;
+  a.st_vc = L.st_vc;
+  a.st_vm = L.st_vm;
+  a.stage_bytes = L.stage_bytes;
+  a.lg_nstages = L.lg_ns;
+  a.barea_bytes = L.barea_bytes;
+  a.canon_k = L.canon_k;
+  a.canon_v = L.canon_v;
+  a.stage_off = L.stage_off;
+  a.warp_bytes = L.warp_bytes;
+  a.head_bytes = L.head_bytes;
+  const size_t smem = (size_t)a.head_bytes + (size_t)kWarps * a.warp_bytes;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int occ = 1;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kWarps * 32, smem);
+  if (e != cudaSuccess) return e;
+  std::vector<int32_t> plan(C->lens.begin() + (long)layer * cfg.batch, C->lens.begin() + (long)(layer + 1) * cfg.batch);
+  for (auto& x : plan) x = std::max(x, (int32_t)std::min(C->plan_tokens, C->cfg.max_tokens));
+  const int slots = C->sm_count * std::min(std::max(occ, 1), 4);
+  a.S = choose_split(C, plan.data(), kTile, slots, C->max_chunks);
+  a.Sw = a.S / kWarps;
+  int maxn = 0;
+  for (int b = 0; b < cfg.batch; ++b) maxn = std::max(maxn, (int)plan[b]);
+  const int nch = std::max(1, (maxn + a.S - 1) / a.S);
+  const long need = (5L * rep * (D + 2) + 2L * rep * kMaxCluster + rep) * 4;
+  const long ctas = (long)nch * cfg.kv_heads * cfg.batch;
+  a.csize = (!C->global_combine && need <= 4L * a.warp_bytes && nch <= kMaxCluster && ctas <= slots) ? nch : 0;
+  a.q = q;
+  a.q_f32 = q_f32;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.out = out;
+  void* args[] = {&a};
+  e = launch_pdl(fn, dim3(nch, cfg.kv_heads, cfg.batch), dim3(kWarps * 32), smem, st, args, a.csize);
+  ++*launches;
+  return e;
+}
+
 }  // namespace kvq

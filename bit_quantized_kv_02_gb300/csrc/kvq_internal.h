@@ -78,6 +78,9 @@ cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v
                            const int32_t* lens_host, long t_stride, cudaStream_t st, int* launches);
 cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, cudaStream_t st,
                           int* launches);
+cudaError_t launch_dequantize(kvq_cache* C, int layer, void* k_out, void* v_out, cudaStream_t st, int* launches);
+cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16, const void* v16, const void* q,
+                                       int q_f32, float scale, float* out, cudaStream_t st, int* launches);
 cudaError_t launch_export(kvq_cache* C, int layer, int is_value, uint8_t* codes, float* meta, uint16_t* tail,
                           cudaStream_t st);
 size_t append_smem(const kvq_cache* C);

@@ -396,8 +396,7 @@ __global__ void append_kernel(const __grid_constant__ AppendArgs a) {
   pdl_trigger();  // the decode that follows may get its CTAs resident now
   const int n = *my_len;
   const QuantArgs& t = warp == 0 ? a.k : a.v;
-  if (threadIdx.x < 2) seal[threadIdx.x] = 0;
-  __syncthreads();
+  bool full = false;
   if (warp < 2 && !(t.L.whole && h != 0)) {
     const int rowlen = (t.L.whole ? t.H : 1) * t.D;
     unsigned char* base = smem + warp * a.warp_smem;
@@ -405,9 +404,9 @@ __global__ void append_kernel(const __grid_constant__ AppendArgs a) {
     float* zs = xs + rowlen;
     float* ss = zs + 16;
     uint8_t* cs = reinterpret_cast<uint8_t*>(ss + 16);
-    const bool full = append_warp(t, b, h, n, xs, cs, zs, ss);
-    if (full && (threadIdx.x & 31) == 0) seal[warp] = 1;
+    full = append_warp(t, b, h, n, xs, cs, zs, ss);
   }
+  if (warp < 2 && (threadIdx.x & 31) == 0) seal[warp] = full ? 1 : 0;
   __syncthreads();
   for (int w = 0; w < 2; ++w) {
     if (!seal[w]) continue;
@@ -502,6 +501,53 @@ __global__ void export_tail_kernel(ExportArgs e) {
   }
 }
 
+// ------------------------------------------------------ materialised path --
+
+// Dequantise one tensor of a layer into fp16 rows out[b][h][t][D] (t < lens[b]):
+// x_hat = z + code * s (asymmetric, one fp32 fma), (code - 2^(B-1)) * s
+// (symmetric), the stored fp16 value for the tail, then rounded to nearest
+// fp16.  This is the "dequantise the cached block into a temporary
+// floating-point tensor before attention" design of "Kuantisasi KV Cache untuk
+// Mengurangi Memory Inferensi Long Context", section "Kuantisasi dapat
+// memindahkan pekerjaan ke decode path", kept as the baseline the fused decode
+// is measured against.  One CTA per (tile, head, sequence).
+__global__ void dequant_kernel(QuantArgs a, __half* out, long t_stride) {
+  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z, D = a.D;
+  const int n = a.lens[b];
+  if (tile * kTile >= n) return;
+  const int ns = sealed_of(a.L, n);
+  const uint32_t* src = codes_ptr(a, b, h, tile);
+  const char* meta = meta_ptr(a);
+  const int G = a.L.whole ? a.H * D : a.L.group;
+  const float soff = (float)(1 << (a.L.bits - 1));
+  __half* dst = out + (((long)b * a.H + h) * t_stride) * D;
+  for (int i = threadIdx.x; i < kTile * D; i += blockDim.x) {
+    const int tt = i / D, c = i % D, t = tile * kTile + tt;
+    if (t >= n) continue;
+    __half v;
+    if (t < ns) {
+      const FragPos f = elem_pos(a.is_value, tt, c);
+      uint32_t code = 0;
+      for (int p = 0; p < a.L.planes.n; ++p) {
+        int word, bit;
+        plane_word_bit(f, D, a.L.planes.w[p], a.L.planes.off[p], &word, &bit);
+        code |= ((src[word] >> bit) & ((1u << a.L.planes.w[p]) - 1u)) << a.L.planes.off[p];
+      }
+      long mi;
+      if (a.L.axis == 1) mi = (((long)b * a.H + h) * (a.tcap / G) + t / G) * D + c;
+      else if (a.L.whole) mi = (long)b * a.tcap + t;
+      else mi = (((long)b * a.H + h) * a.tcap + t) * a.L.gpt + c / G;
+      float z, st;
+      load_meta(meta, mi, a.L.meta_f32, a.L.sym, &z, &st);
+      const float x = a.L.sym ? ((float)code - soff) * st : __fmaf_rn((float)code, st, z);
+      v = __float2half_rn(x);
+    } else {
+      v = tail_ptr(a, b, h)[(long)(t - ns) * D + c];
+    }
+    dst[(long)t * D + c] = v;
+  }
+}
+
 // ------------------------------------------------------------- launchers ---
 
 static QuantArgs make_args(const kvq_cache* C, int is_value, int layer, const void* x, int x_f32, long t_stride) {
@@ -577,6 +623,22 @@ size_t append_smem(const kvq_cache* C) {
   for (int i = 0; i < 2; ++i)
     if (ls[i]->axis == 1) m = std::max(m, channel_smem(ls[i]->group, C->cfg.head_dim));
   return m;
+}
+
+cudaError_t launch_dequantize(kvq_cache* C, int layer, void* k_out, void* v_out, cudaStream_t st, int* launches) {
+  const int B = C->cfg.batch, H = C->cfg.kv_heads;
+  int maxn = 0;
+  // host mirror raised to the plan hint, as for decode (CTAs past a length exit)
+  for (int b = 0; b < B; ++b)
+    maxn = std::max(maxn, std::max((int)C->lens[(long)layer * B + b], std::min(C->plan_tokens, C->cfg.max_tokens)));
+  if (maxn == 0) return cudaSuccess;
+  for (int is_v = 0; is_v < 2; ++is_v) {
+    QuantArgs a = make_args(C, is_v, layer, nullptr, 0, 0);
+    dequant_kernel<<<dim3((maxn + kTile - 1) / kTile, H, B), 128, 0, st>>>(
+        a, static_cast<__half*>(is_v ? v_out : k_out), C->cfg.max_tokens);
+    ++*launches;
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, cudaStream_t st,

@@ -57,7 +57,7 @@ EXPORTED = ["kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_pre
             "kvq_decode_attn", "kvq_export", "kvq_cache_tcap", "kvq_get_lens", "kvq_decode_traffic",
             "kvq_device_status", "kvq_last_launches", "kvq_status_string", "kvq_last_error",
             "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static", "kvq_set_decode_kernel",
-            "kvq_decode_kernel_specialized"]
+            "kvq_decode_kernel_specialized", "kvq_dequantize", "kvq_decode_attn_materialized"]
 
 
 def lib():
@@ -87,6 +87,8 @@ def lib():
         L.kvq_status_string.argtypes = [S]
         L.kvq_status_string.restype = ctypes.c_char_p
         L.kvq_decode_attn_static.argtypes = [P, I, P, I, ctypes.c_float, P, P]
+        L.kvq_dequantize.argtypes = [P, I, P, P, P]
+        L.kvq_decode_attn_materialized.argtypes = [P, I, P, P, P, I, ctypes.c_float, P, P]
         L.kvq_set_decode_plan.argtypes = [P, I]
         L.kvq_set_decode_kernel.argtypes = [P, I]
         L.kvq_decode_kernel_specialized.argtypes = [P]
@@ -97,7 +99,7 @@ def lib():
         for name in ("kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_prefill_quantize",
                      "kvq_append", "kvq_decode_attn", "kvq_export", "kvq_get_lens", "kvq_decode_traffic",
                      "kvq_device_status", "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static",
-                     "kvq_set_decode_kernel"):
+                     "kvq_set_decode_kernel", "kvq_dequantize", "kvq_decode_attn_materialized"):
             getattr(L, name).restype = S
         _lib = L
         return L
@@ -209,6 +211,35 @@ class KVQCache:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         _check(lib().kvq_decode_attn_static(self.handle, layer, _ptr(q), _dtype_code(q), float(scale), _ptr(out),
                                             _stream(stream)), "kvq_decode_attn_static", self.handle)
+        return out
+
+    def kvq_dequantize(self, layer: int, k_out: torch.Tensor | None = None, v_out: torch.Tensor | None = None,
+                       stream=None):
+        """Materialised baseline: fp16 K and V rows [batch][kv_heads][max_tokens][head_dim]
+        of `layer` (rows past a sequence's length are left as they were)."""
+        c = self.cfg
+        shape = (c.batch, c.kv_heads, c.max_tokens, c.head_dim)
+        if k_out is None:
+            k_out = torch.zeros(shape, dtype=torch.float16, device=self.buffer.device)
+        if v_out is None:
+            v_out = torch.zeros(shape, dtype=torch.float16, device=self.buffer.device)
+        assert k_out.shape == shape and v_out.shape == shape and k_out.dtype == torch.float16
+        assert k_out.is_contiguous() and v_out.is_contiguous() and v_out.dtype == torch.float16
+        _check(lib().kvq_dequantize(self.handle, layer, _ptr(k_out), _ptr(v_out), _stream(stream)), "kvq_dequantize",
+               self.handle)
+        return k_out, v_out
+
+    def kvq_decode_attn_materialized(self, layer: int, k16: torch.Tensor, v16: torch.Tensor, q: torch.Tensor,
+                                     out: torch.Tensor | None = None, scale: float = 0.0,
+                                     stream=None) -> torch.Tensor:
+        """Decode attention over rows from kvq_dequantize (the baseline the fused
+        kvq_decode_attn is measured against); same query and output layout."""
+        assert q.is_contiguous() and k16.is_contiguous() and v16.is_contiguous()
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        _check(lib().kvq_decode_attn_materialized(self.handle, layer, _ptr(k16), _ptr(v16), _ptr(q), _dtype_code(q),
+                                                  float(scale), _ptr(out), _stream(stream)),
+               "kvq_decode_attn_materialized", self.handle)
         return out
 
     def kvq_export(self, layer: int, stream=None) -> dict:

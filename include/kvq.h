@@ -193,6 +193,28 @@ int kvq_cache_tcap(kvq_cache_t cache);
 /* Host mirror of the lengths of layer `layer` (lens_host: int32[batch]). */
 kvq_status kvq_get_lens(kvq_cache_t cache, int layer, int32_t* lens_host);
 
+/* Materialised baseline, step 1: dequantize layer `layer` into fp16 rows
+ * k_out, v_out [batch][kv_heads][max_tokens][head_dim] (device; caller-owned;
+ * token t of sequence b at row t; rows >= the sequence's length are not
+ * written): x_hat = z + code * s as one fp32 fma (asymmetric), (code -
+ * 2^(B-1)) * s (symmetric), the stored fp16 value for tail tokens, rounded to
+ * nearest fp16.  This is the design that dequantizes a cached block into a
+ * temporary floating-point tensor before attention ("Kuantisasi KV Cache untuk
+ * Mengurangi Memory Inferensi Long Context", section "Kuantisasi dapat
+ * memindahkan pekerjaan ke decode path"); it exists to measure the fused
+ * kvq_decode_attn against.  Asynchronous on `stream`; KVQ_ERR_INVALID_ARG for
+ * a bad layer or null output. */
+kvq_status kvq_dequantize(kvq_cache_t cache, int layer, void* k_out, void* v_out, void* stream);
+
+/* Materialised baseline, step 2: decode attention (same definition, query
+ * layout, scale and output as kvq_decode_attn) over fp16 rows k16, v16 in the
+ * kvq_dequantize layout, for the lengths of `layer` in `cache`.  Uses the same
+ * split-K kernel with every token read as fp16 (no packed codes, no metadata)
+ * and the cache's workspace, so it must not overlap a kvq_decode_attn on the
+ * same cache. */
+kvq_status kvq_decode_attn_materialized(kvq_cache_t cache, int layer, const void* k16, const void* v16,
+                                        const void* q, int q_dtype, float softmax_scale, float* out, void* stream);
+
 /* Bytes one kvq_decode_attn call on `layer` must read at minimum with the
  * current lengths: packed codes + metadata + fp16 tail + q (q_dtype bytes per
  * element), the algorithmic traffic of the path.  Host only. */

@@ -158,6 +158,52 @@ def test_specialized_and_generic_kernels(case, generic):
     run_case(wl, lens, generic=generic)
 
 
+def _ord16(h):
+    """fp16 values as integers whose differences count ulps (sign-magnitude -> ordered)."""
+    u = np.asarray(h, np.float16).view(np.uint16).astype(np.int32)
+    return np.where(u & 0x8000, -(u & 0x7FFF), u)
+
+
+MAT_CASES = [CASES[0], CASES[6], CASES[7], CASES[11], CASES[14], CASES[15], FAST_CASES[2]]
+
+
+@pytest.mark.parametrize("case", MAT_CASES, ids=[c[0] for c in MAT_CASES])
+def test_materialized_baseline(case):
+    """kvq_dequantize writes the oracle's dequantized cache rounded to fp16
+    (within one fp16 ulp: the GPU rounds its one-rounding fp32 value, the oracle
+    an exact one), and kvq_decode_attn_materialized over those rows agrees with
+    the oracle's attention over the unrounded cache within the path's
+    tolerance."""
+    name, B, Hq, H, D, kc, vc, lens = case
+    wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=21)
+    T = max(max(lens), 1)
+    cache = make_cache(wl, max_tokens=T)
+    k, v = wl.layer_kv(0, "cpu", T=T)
+    cache.kvq_prefill_quantize(0, k.cuda(), v.cuda(), lens)
+    k16, v16 = cache.kvq_dequantize(0)
+    q = wl.layer_query(0)
+    scale = np.float32(1.0 / np.sqrt(D))
+    out = cache.kvq_decode_attn_materialized(0, k16, v16, q.cuda(), scale=float(scale))
+    torch.cuda.synchronize()
+    assert cache.kvq_device_status() == 0
+    ok = oracle_tensor(k, lens, cache.tcap, wl.k, False)
+    ov = oracle_tensor(v, lens, cache.tcap, wl.v, False)
+    kh = oracle.dequant_tensor(ok, lens, wl.k[0], wl.k[1], wl.k[2], bool(wl.k[3]))
+    vh = oracle.dequant_tensor(ov, lens, wl.v[0], wl.v[1], wl.v[2], bool(wl.v[3]))
+    for gpu, ref, which in ((k16, kh, "k"), (v16, vh, "v")):
+        g = gpu.cpu().numpy()
+        for b, n in enumerate(lens):
+            d = np.abs(_ord16(g[b, :, :n]) - _ord16(ref[b, :, :n].astype(np.float16)))
+            assert d.size == 0 or d.max() <= 1, (which, b, d.max())
+    ref_out = oracle.attention(kh, vh, q.float().numpy(), np.array(lens, np.int32), scale)
+    err = rel_err_rows(out.cpu().numpy(), ref_out)
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert not out[b].any()
+            err[b] = 0.0
+    assert err.max() <= TOL, err.max()
+
+
 GLOBAL_COMBINE_CASES = [CASES[0], CASES[11], FAST_CASES[0], FAST_CASES[2], FAST_CASES[6]]
 
 
