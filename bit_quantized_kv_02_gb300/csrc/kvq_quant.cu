@@ -16,6 +16,7 @@
 // with 128-bit stores where a thread owns four consecutive words.
 #include <algorithm>
 
+#include "kvq_decode.cuh"
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -141,6 +142,7 @@ __device__ __forceinline__ uint32_t* codes_ptr(const QuantArgs& a, int b, int h,
 __device__ __forceinline__ char* meta_ptr(const QuantArgs& a) {
   return a.base + a.L.meta_off + a.layer * a.L.meta_layer;
 }
+__device__ __forceinline__ long bh_of(const QuantArgs& a, int b, int h) { return (long)b * a.H + h; }
 __device__ __forceinline__ __half* tail_ptr(const QuantArgs& a, int b, int h) {
   return reinterpret_cast<__half*>(a.base + a.L.tail_off + a.layer * a.L.tail_layer) +
          (((long)b * a.H + h) * a.L.group) * a.D;
@@ -510,41 +512,83 @@ __global__ void export_tail_kernel(ExportArgs e) {
 // floating-point tensor before attention" design of "Kuantisasi KV Cache untuk
 // Mengurangi Memory Inferensi Long Context", section "Kuantisasi dapat
 // memindahkan pekerjaan ke decode path", kept as the baseline the fused decode
-// is measured against.  One CTA per (tile, head, sequence).
-__global__ void dequant_kernel(QuantArgs a, __half* out, long t_stride) {
-  const int tile = blockIdx.x, h = blockIdx.y, b = blockIdx.z, D = a.D;
+// is measured against.  One CTA per (tile, head, sequence): each warp turns
+// whole 16-channel chunks into exact fp16 codes with the decode path's
+// register conversion, applies the group's zero point and step per element
+// into a shared tile, and the CTA writes the tile's valid rows with 16-byte
+// stores.
+template <int D>
+__global__ void __launch_bounds__(128) dequant_kernel(QuantArgs a, __half* out, long t_stride) {
+  // one 16-token tile per warp, four consecutive tiles per CTA
+  __shared__ __align__(16) __half tileo[kWarps][kTile * D];
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+  const int tile = blockIdx.x * kWarps + warp;
   const int n = a.lens[b];
-  if (tile * kTile >= n) return;
+  const int t_base = tile * kTile;
+  if (t_base >= n) return;
   const int ns = sealed_of(a.L, n);
-  const uint32_t* src = codes_ptr(a, b, h, tile);
-  const char* meta = meta_ptr(a);
-  const int G = a.L.whole ? a.H * D : a.L.group;
-  const float soff = (float)(1 << (a.L.bits - 1));
-  __half* dst = out + (((long)b * a.H + h) * t_stride) * D;
-  for (int i = threadIdx.x; i < kTile * D; i += blockDim.x) {
-    const int tt = i / D, c = i % D, t = tile * kTile + tt;
-    if (t >= n) continue;
-    __half v;
-    if (t < ns) {
-      const FragPos f = elem_pos(a.is_value, tt, c);
-      uint32_t code = 0;
-      for (int p = 0; p < a.L.planes.n; ++p) {
-        int word, bit;
-        plane_word_bit(f, D, a.L.planes.w[p], a.L.planes.off[p], &word, &bit);
-        code |= ((src[word] >> bit) & ((1u << a.L.planes.w[p]) - 1u)) << a.L.planes.off[p];
+  __half* to = tileo[warp];
+  if (t_base < ns) {
+    const uint32_t* src = codes_ptr(a, b, h, tile);
+    const char* meta = meta_ptr(a);
+    const int bits = a.L.bits;
+    const int cg = conv_g(bits), cr = conv_r(bits), cc = conv_c(bits);
+    const float off = (float)conv_off(bits), soff = (float)(1 << (bits - 1));
+    const int G = a.L.whole ? a.H * D : a.L.group;
+    const int lgG = 31 - __clz(G);
+    const long bh = (long)b * a.H + h;
+    for (int j = 0; j < D / 16; ++j) {
+      uint32_t A[4];
+      convert_dispatch<D>(bits, src, lane, j, A);
+      // the lane's 8 elements share 4 metadata entries: keys (rows = tokens) need
+      // channels 2tig, 2tig+1, 2tig+8, 2tig+9 of the chunk (per-channel) or the
+      // group of each row token (per-token); values (rows = channels) need
+      // tokens 2tig, 2tig+1, 2tig+8, 2tig+9 (per-token) or the two row channels
+      float mz[4], ms[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int kk = 2 * tig + (m & 1) + 8 * (m >> 1);  // column of entry m
+        long mi;
+        if (a.L.axis == 1) {
+          // per-channel: entry per column channel (keys) or row channel (values)
+          const int c = a.is_value ? 16 * j + g + 8 * (m & 1) : 16 * j + kk;
+          mi = (bh * (a.tcap >> lgG) + (t_base >> lgG)) * D + c;
+        } else {
+          // per-token: entry per column token (values) or row token (keys)
+          const long ta = t_base + (a.is_value ? kk : g + 8 * (m & 1));
+          const int c = a.is_value ? 16 * j + g : 16 * j + kk;
+          mi = a.L.whole ? (long)b * a.tcap + ta : (bh * a.tcap + ta) * a.L.gpt + (c >> lgG);
+        }
+        load_meta(meta, mi, a.L.meta_f32, a.L.sym, &mz[m], &ms[m]);
       }
-      long mi;
-      if (a.L.axis == 1) mi = (((long)b * a.H + h) * (a.tcap / G) + t / G) * D + c;
-      else if (a.L.whole) mi = (long)b * a.tcap + t;
-      else mi = (((long)b * a.H + h) * a.tcap + t) * a.L.gpt + c / G;
-      float z, st;
-      load_meta(meta, mi, a.L.meta_f32, a.L.sym, &z, &st);
-      const float x = a.L.sym ? ((float)code - soff) * st : __fmaf_rn((float)code, st, z);
-      v = __float2half_rn(x);
-    } else {
-      v = tail_ptr(a, b, h)[(long)(t - ns) * D + c];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float unscale = exp2i(-(cg + cr * (r & 1) + cc * (r >> 1)));
+        const __half2 hv = *reinterpret_cast<const __half2*>(&A[r]);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int R = g + 8 * (r & 1), kk = 2 * tig + 8 * (r >> 1) + e;
+          const int t = a.is_value ? kk : R, c = 16 * j + (a.is_value ? R : kk);
+          // entry index: the column (e, column half) for per-channel keys and
+          // per-token values, the row (row half) otherwise
+          const bool by_col = (a.L.axis == 1) != (a.is_value != 0);
+          const int m = by_col ? (e + 2 * (r >> 1)) : (r & 1);
+          const float code = (e ? __high2float(hv) : __low2float(hv)) * unscale - off;
+          const float x = a.L.sym ? (code - soff) * ms[m] : __fmaf_rn(code, ms[m], mz[m]);
+          to[t * D + c] = __float2half_rn(x);
+        }
+      }
     }
-    dst[(long)t * D + c] = v;
+  }
+  __syncwarp();
+  __half* dst = out + ((bh_of(a, b, h)) * t_stride + t_base) * D;
+  for (int i = lane; i < kTile * D / 8; i += 32) {
+    const int t = (i * 8) / D, c = (i * 8) % D, ta = t_base + t;
+    if (ta >= n) continue;
+    const uint4 v = ta < ns ? *reinterpret_cast<const uint4*>(to + t * D + c)
+                            : *reinterpret_cast<const uint4*>(tail_ptr(a, b, h) + (long)(ta - ns) * D + c);
+    *reinterpret_cast<uint4*>(dst + (long)t * D + c) = v;
   }
 }
 
@@ -634,8 +678,12 @@ cudaError_t launch_dequantize(kvq_cache* C, int layer, void* k_out, void* v_out,
   if (maxn == 0) return cudaSuccess;
   for (int is_v = 0; is_v < 2; ++is_v) {
     QuantArgs a = make_args(C, is_v, layer, nullptr, 0, 0);
-    dequant_kernel<<<dim3((maxn + kTile - 1) / kTile, H, B), 128, 0, st>>>(
-        a, static_cast<__half*>(is_v ? v_out : k_out), C->cfg.max_tokens);
+    const dim3 grid((maxn + kTile * kWarps - 1) / (kTile * kWarps), H, B);
+    __half* o = static_cast<__half*>(is_v ? v_out : k_out);
+    const int D = C->cfg.head_dim;
+    if (D == 64) dequant_kernel<64><<<grid, 128, 0, st>>>(a, o, C->cfg.max_tokens);
+    else if (D == 128) dequant_kernel<128><<<grid, 128, 0, st>>>(a, o, C->cfg.max_tokens);
+    else dequant_kernel<256><<<grid, 128, 0, st>>>(a, o, C->cfg.max_tokens);
     ++*launches;
   }
   return cudaGetLastError();

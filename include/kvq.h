@@ -194,7 +194,7 @@ int kvq_cache_tcap(kvq_cache_t cache);
 kvq_status kvq_get_lens(kvq_cache_t cache, int layer, int32_t* lens_host);
 
 /* Materialised baseline, step 1: dequantize layer `layer` into fp16 rows
- * k_out, v_out [batch][kv_heads][max_tokens][head_dim] (device; caller-owned;
+ * k_out, v_out [batch][kv_heads][max_tokens][head_dim] (device, 16-byte aligned; caller-owned;
  * token t of sequence b at row t; rows >= the sequence's length are not
  * written): x_hat = z + code * s as one fp32 fma (asymmetric), (code -
  * 2^(B-1)) * s (symmetric), the stored fp16 value for tail tokens, rounded to
