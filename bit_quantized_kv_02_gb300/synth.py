@@ -75,6 +75,30 @@ def query(B, Hq, D, seed, device="cpu", dtype=torch.float16) -> torch.Tensor:
     return normal((B, Hq, D), seed, device, dtype)
 
 
+def axis_study_inputs(T=1024, H=4, D=128, seed=0, outliers_per_head=2, outlier_scale=15.0, important_frac=0.05,
+                      align=0.42, important_value_scale=0.1, value_channel_spread=0.5):
+    """Inputs of the quantization-axis study: keys N(0,1) with fixed outlier
+    channels (scaled up, the same channels for every token); a query per head;
+    a small set of important tokens whose keys lean towards the query, so
+    that a softmax over q.k/sqrt(D) puts most of its mass on them (sparse
+    attention); values N(0,1) times a mild fixed per-channel scale drawn from
+    [1 - spread, 1 + spread] (no extreme channels), except the important
+    tokens' values, which are scaled down.  Returns (k [1][T][H][D],
+    v [1][T][H][D], q [1][H][D], the important-token mask [T]), fp32 tensors."""
+    mask = outlier_channels(H, D, per_head=outliers_per_head, seed=seed * 1000 + 1)
+    k = keys(1, T, H, D, seed * 1000 + 2, dtype=torch.float32, outlier_mask=mask, outlier_scale=outlier_scale)
+    q = query(1, H, D, seed * 1000 + 3, dtype=torch.float32)
+    g = _gen(seed * 1000 + 4, "cpu")
+    imp = torch.zeros(T, dtype=torch.bool)
+    imp[torch.randperm(T, generator=g)[:max(1, int(round(important_frac * T)))]] = True
+    k[0, imp] += align * q[0][None]
+    v = values(1, T, H, D, seed * 1000 + 5, dtype=torch.float32)
+    cs = 1.0 + value_channel_spread * (2.0 * torch.rand((H, D), generator=g) - 1.0)
+    v = v * cs[None, None]
+    v[0, imp] *= important_value_scale
+    return k, v, q, imp
+
+
 def ragged_lengths(B, lo, hi, seed) -> list:
     g = _gen(seed, "cpu")
     return torch.randint(lo, hi + 1, (B,), generator=g).tolist()
