@@ -68,17 +68,19 @@ def _load():
         lib.kvqo_quant_group.argtypes = [P, L, L, I, I, I, P, L, P, P]
         lib.kvqo_dequant_one.argtypes = [I, F, F, I, I]
         lib.kvqo_dequant_one.restype = ctypes.c_double
-        lib.kvqo_sealed.argtypes = [L, I, I]
+        lib.kvqo_sealed.argtypes = [L, I, I, I]
         lib.kvqo_sealed.restype = L
+        lib.kvqo_tail_rows.argtypes = [I, I, I]
+        lib.kvqo_tail_rows.restype = L
         lib.kvqo_meta_groups.argtypes = [I, I, I, I, I, I]
         lib.kvqo_meta_groups.restype = L
-        lib.kvqo_quantize_tensor.argtypes = [P, I, I, I, I, P, I, I, I, I, I, I, P, P, P]
+        lib.kvqo_quantize_tensor.argtypes = [P, I, I, I, I, P, I, I, I, I, I, I, I, P, P, P]
         lib.kvqo_quantize_tensor.restype = I
-        lib.kvqo_dequant_tensor.argtypes = [P, P, P, I, I, I, P, I, I, I, I, I, P]
+        lib.kvqo_dequant_tensor.argtypes = [P, P, P, I, I, I, P, I, I, I, I, I, I, P]
         lib.kvqo_dequant_tensor.restype = I
         lib.kvqo_attention.argtypes = [P, P, P, P, I, I, I, I, I, F, P]
         lib.kvqo_attention.restype = I
-        lib.kvqo_tensor_bytes.argtypes = [I, I, I, P, I, I, I, I, I, P]
+        lib.kvqo_tensor_bytes.argtypes = [I, I, I, P, I, I, I, I, I, I, P]
         lib.kvqo_cache_elements.argtypes = [I, ctypes.c_double, I, I]
         lib.kvqo_cache_elements.restype = ctypes.c_double
         _lib = lib
@@ -126,8 +128,14 @@ def resolve_group(group: int, heads: int, dim: int) -> int:
     return heads * dim if group == WHOLE_VECTOR else group
 
 
-def sealed(n: int, axis: int, group: int) -> int:
-    return _load().kvqo_sealed(n, axis, group)
+def sealed(n: int, axis: int, group: int, window: int = 0) -> int:
+    """Tokens of a length-n sequence held as codes (the rest stay fp16)."""
+    return _load().kvqo_sealed(n, axis, group, window)
+
+
+def tail_rows(axis: int, group: int, window: int = 0) -> int:
+    """fp16 rows per (sequence, head) the unsealed tokens can occupy."""
+    return _load().kvqo_tail_rows(axis, group, window)
 
 
 def meta_groups(batch, heads, dim, tcap, axis, group) -> int:
@@ -135,28 +143,31 @@ def meta_groups(batch, heads, dim, tcap, axis, group) -> int:
 
 
 def quantize_tensor(x, lens, tcap: int, bits: int, group: int, axis: int, sym: bool = False,
-                    meta_f32: bool = False):
+                    meta_f32: bool = False, window: int = 0):
     """Quantize one layer-tensor.
 
     x: float array [batch][T][heads][dim] (exact fp32 copies of the source values);
-    lens: int [batch].  Returns dict(codes [B][H][tcap][D] uint8, meta [groups][2] f32,
-    tail [B][H][G][D] uint16 fp16 bits or None)."""
+    lens: int [batch]; window: full-precision recent tokens (multiple of 16, 0 = none).
+    Returns dict(codes [B][H][tcap][D] uint8, meta [groups][2] f32, tail
+    [B][H][tail_rows][D] uint16 fp16 bits of the unsealed tokens (row t - sealed)
+    or None when the tensor has no fp16 rows)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     batch, tstride, heads, dim = x.shape
     lens = np.ascontiguousarray(lens, dtype=np.int32)
     g = resolve_group(group, heads, dim)
     codes = np.empty((batch, heads, tcap, dim), dtype=np.uint8)
     meta = np.empty((meta_groups(batch, heads, dim, tcap, axis, g), 2), dtype=np.float32)
-    tail = np.zeros((batch, heads, g, dim), dtype=np.uint16) if axis == PER_CHANNEL else None
+    rows = tail_rows(axis, g, window)
+    tail = np.zeros((batch, heads, rows, dim), dtype=np.uint16) if rows else None
     rc = _load().kvqo_quantize_tensor(_ptr(x), batch, tstride, heads, dim, _ptr(lens), tcap, bits, g, axis,
-                                      int(sym), int(meta_f32), _ptr(codes), _ptr(meta),
+                                      int(sym), int(meta_f32), int(window), _ptr(codes), _ptr(meta),
                                       _ptr(tail) if tail is not None else None)
     if rc != 0:
         raise ValueError("oracle: unsupported tensor shape/config")
     return {"codes": codes, "meta": meta, "tail": tail}
 
 
-def dequant_tensor(q, lens, bits: int, group: int, axis: int, sym: bool = False) -> np.ndarray:
+def dequant_tensor(q, lens, bits: int, group: int, axis: int, sym: bool = False, window: int = 0) -> np.ndarray:
     """Reconstruct x_hat [B][H][tcap][D] (float64) from quantize_tensor()'s output."""
     codes, meta, tail = q["codes"], q["meta"], q["tail"]
     batch, heads, tcap, dim = codes.shape
@@ -165,7 +176,8 @@ def dequant_tensor(q, lens, bits: int, group: int, axis: int, sym: bool = False)
     out = np.empty(codes.shape, dtype=np.float64)
     rc = _load().kvqo_dequant_tensor(_ptr(np.ascontiguousarray(codes)), _ptr(np.ascontiguousarray(meta)),
                                      _ptr(np.ascontiguousarray(tail)) if tail is not None else None,
-                                     batch, heads, dim, _ptr(lens), tcap, bits, g, axis, int(sym), _ptr(out))
+                                     batch, heads, dim, _ptr(lens), tcap, bits, g, axis, int(sym), int(window),
+                                     _ptr(out))
     if rc != 0:
         raise ValueError("oracle: dequant failed (missing tail?)")
     return out
@@ -188,12 +200,12 @@ def attention(khat, vhat, q, lens, scale: float) -> np.ndarray:
     return out
 
 
-def tensor_bytes(batch, heads, dim, lens, bits, group, axis, sym=False, meta_f32=False):
+def tensor_bytes(batch, heads, dim, lens, bits, group, axis, sym=False, meta_f32=False, window=0):
     """(packed, metadata, tail) bytes of one layer-tensor holding lens tokens."""
     lens = np.ascontiguousarray(lens, dtype=np.int32)
     out = np.zeros(3, dtype=np.float64)
     _load().kvqo_tensor_bytes(batch, heads, dim, _ptr(lens), bits, resolve_group(group, heads, dim), axis,
-                              int(sym), int(meta_f32), _ptr(out))
+                              int(sym), int(meta_f32), int(window), _ptr(out))
     return tuple(float(v) for v in out)
 
 

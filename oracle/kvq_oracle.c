@@ -42,7 +42,16 @@
  *    stored code is q + 2^(B-1);
  *  - the fp16 recent-token tail holds the input rounded to nearest fp16, and a
  *    per-channel group is quantized from those fp16 values (so a prefill and a
- *    token-by-token append of the same tokens build the same cache).
+ *    token-by-token append of the same tokens build the same cache);
+ *  - full-precision recent window of R tokens for both tensors (same page,
+ *    section "O Imposto dos Sistemas e Por Que Nao E um Detalhe": the most
+ *    recent tokens, up to 128, stay in full precision and are quantized in
+ *    groups once enough have accumulated): with R > 0 a per-channel group is
+ *    sealed once all its tokens are older than the newest R, and a per-token
+ *    tensor quantizes a 16-token block once all of it is older than the newest
+ *    R (tokens in between stay fp16); tokens quantized after a stay in the
+ *    window are quantized from their fp16 values.  R = 0 is the cache without
+ *    a window (per-token tensors quantize every token on arrival).
  */
 #include <math.h>
 #include <stdint.h>
@@ -202,9 +211,18 @@ double kvqo_dequant_one(int code, float z, float s, int bits, int sym) {
 
 /* ------------------------------------------------ layer-level tensors ----- */
 
-/* Number of tokens of a sequence of length n whose codes are sealed. */
-long kvqo_sealed(long n, int axis, int group) {
-  return axis == KVQO_PER_CHANNEL ? (n / group) * group : n;
+/* Number of tokens of a sequence of length n whose codes are sealed, with a
+ * full-precision window of the newest `window` tokens (0: none). */
+long kvqo_sealed(long n, int axis, int group, int window) {
+  long old = n - window > 0 ? n - window : 0;
+  if (axis == KVQO_PER_CHANNEL) return (old / group) * group;
+  return window ? (old / 16) * 16 : n;
+}
+
+/* fp16 rows per (sequence, head) that the unsealed tokens can occupy. */
+long kvqo_tail_rows(int axis, int group, int window) {
+  if (axis == KVQO_PER_CHANNEL) return (long)group + window;
+  return window ? (long)window + 16 : 0;
 }
 
 /* Number of metadata groups in the canonical layout of one layer. */
@@ -222,13 +240,15 @@ long kvqo_meta_groups(int batch, int heads, int dim, int tcap, int axis, int gro
  *           per channel : ((b*heads + h)*(tcap/G) + t/G)*dim + c
  *           per token   : ((b*heads + h)*tcap + t)*(dim/G) + c/G
  *           whole vector: b*tcap + t
- *   tail  : [batch][heads][group][dim] fp16 bits of the unsealed tokens of a
- *           per-channel tensor (slot = t - sealed), or NULL.
+ *   tail  : [batch][heads][tail_rows][dim] fp16 bits of the unsealed tokens
+ *           (slot = t - sealed; tail_rows = kvqo_tail_rows()), or NULL when
+ *           there are none.
  * Returns 0, or -1 on an unsupported shape. */
 int kvqo_quantize_tensor(const float* x, int batch, int tstride, int heads, int dim, const int* lens, int tcap,
-                         int bits, int group, int axis, int sym, int meta_f32, uint8_t* codes, float* meta,
+                         int bits, int group, int axis, int sym, int meta_f32, int window, uint8_t* codes, float* meta,
                          uint16_t* tail) {
-  if (bits < 2 || bits > 8) return -1;
+  if (bits < 2 || bits > 8 || window < 0 || window % 16) return -1;
+  const long rows = kvqo_tail_rows(axis, group, window);
   const long xs_t = (long)heads * dim;      /* stride between tokens */
   const long xs_b = (long)tstride * xs_t;   /* stride between sequences */
   memset(codes, 0, sizeof(uint8_t) * (size_t)batch * heads * tcap * dim);
@@ -237,8 +257,18 @@ int kvqo_quantize_tensor(const float* x, int batch, int tstride, int heads, int 
     long n = lens[b];
     if (n > tcap || n > tstride) return -1;
     const float* xb = x + b * xs_b;
+    const long ns = kvqo_sealed(n, axis, group, window);
+    /* unsealed tokens: the input rounded to nearest fp16 */
+    if (ns < n) {
+      if (!tail) return -1;
+      for (int h = 0; h < heads; ++h)
+        for (long t = ns; t < n; ++t)
+          for (int c = 0; c < dim; ++c)
+            tail[(((long)b * heads + h) * rows + (t - ns)) * dim + c] =
+                kvqo_f32_to_f16(xb[t * xs_t + (long)h * dim + c], KVQO_ROUND_NEAREST);
+    }
     if (axis == KVQO_PER_CHANNEL) {
-      long ng = n / group;
+      long ng = ns / group;
       float* col = (float*)malloc(sizeof(float) * (size_t)group);
       for (int h = 0; h < heads; ++h) {
         for (long g = 0; g < ng; ++g) {
@@ -253,64 +283,66 @@ int kvqo_quantize_tensor(const float* x, int batch, int tstride, int heads, int 
             kvqo_quant_group(col, group, 1, bits, sym, meta_f32, dst, dim, &meta[2 * mi], &meta[2 * mi + 1]);
           }
         }
-        if (tail) {
-          for (long t = ng * group; t < n; ++t) {
-            for (int c = 0; c < dim; ++c) {
-              float v = xb[t * xs_t + (long)h * dim + c];
-              tail[(((long)b * heads + h) * group + (t - ng * group)) * dim + c] =
-                  kvqo_f32_to_f16(v, KVQO_ROUND_NEAREST);
-            }
-          }
-        }
       }
       free(col);
     } else if (group == heads * dim) {
-      for (long t = 0; t < n; ++t) {
-        /* the whole token vector (all heads) is one group; codes land per head */
+      float* vec = (float*)malloc(sizeof(float) * (size_t)heads * dim);
+      for (long t = 0; t < ns; ++t) {
+        /* the whole token vector (all heads) is one group; codes land per head.
+           After a stay in the window the token is quantized from its fp16 values. */
+        for (long i = 0; i < (long)heads * dim; ++i) {
+          float v = xb[t * xs_t + i];
+          vec[i] = window ? kvqo_f16_to_f32(kvqo_f32_to_f16(v, KVQO_ROUND_NEAREST)) : v;
+        }
         uint8_t* tmp = (uint8_t*)malloc((size_t)heads * dim);
         long mi = (long)b * tcap + t;
-        kvqo_quant_group(xb + t * xs_t, (long)heads * dim, 1, bits, sym, meta_f32, tmp, 1, &meta[2 * mi],
-                         &meta[2 * mi + 1]);
+        kvqo_quant_group(vec, (long)heads * dim, 1, bits, sym, meta_f32, tmp, 1, &meta[2 * mi], &meta[2 * mi + 1]);
         for (int h = 0; h < heads; ++h)
           for (int c = 0; c < dim; ++c)
             codes[(((long)b * heads + h) * tcap + t) * dim + c] = tmp[(long)h * dim + c];
         free(tmp);
       }
+      free(vec);
     } else {
       if (dim % group) return -1;
       int gpd = dim / group;
-      for (long t = 0; t < n; ++t) {
+      float* vec = (float*)malloc(sizeof(float) * (size_t)group);
+      for (long t = 0; t < ns; ++t) {
         for (int h = 0; h < heads; ++h) {
           for (int j = 0; j < gpd; ++j) {
             const float* src = xb + t * xs_t + (long)h * dim + (long)j * group;
+            for (int i = 0; i < group; ++i)
+              vec[i] = window ? kvqo_f16_to_f32(kvqo_f32_to_f16(src[i], KVQO_ROUND_NEAREST)) : src[i];
             uint8_t* dst = codes + (((long)b * heads + h) * tcap + t) * dim + (long)j * group;
             long mi = (((long)b * heads + h) * tcap + t) * gpd + j;
-            kvqo_quant_group(src, group, 1, bits, sym, meta_f32, dst, 1, &meta[2 * mi], &meta[2 * mi + 1]);
+            kvqo_quant_group(vec, group, 1, bits, sym, meta_f32, dst, 1, &meta[2 * mi], &meta[2 * mi + 1]);
           }
         }
       }
+      free(vec);
     }
   }
   return 0;
 }
 
 /* Reconstruct one tensor of one layer into xhat [batch][heads][tcap][dim]
- * (double): sealed tokens from codes and metadata, unsealed tokens of a
- * per-channel tensor from the fp16 tail, tokens >= lens[b] set to 0. */
+ * (double): sealed tokens from codes and metadata, unsealed tokens from the
+ * fp16 tail, tokens >= lens[b] set to 0. */
 int kvqo_dequant_tensor(const uint8_t* codes, const float* meta, const uint16_t* tail, int batch, int heads,
-                        int dim, const int* lens, int tcap, int bits, int group, int axis, int sym,
+                        int dim, const int* lens, int tcap, int bits, int group, int axis, int sym, int window,
                         double* xhat) {
   memset(xhat, 0, sizeof(double) * (size_t)batch * heads * tcap * dim);
+  const long rows = kvqo_tail_rows(axis, group, window);
   for (int b = 0; b < batch; ++b) {
     long n = lens[b];
-    long ns = kvqo_sealed(n, axis, group);
+    long ns = kvqo_sealed(n, axis, group, window);
     for (int h = 0; h < heads; ++h) {
       for (long t = 0; t < n; ++t) {
         for (int c = 0; c < dim; ++c) {
           long o = (((long)b * heads + h) * tcap + t) * dim + c;
           if (t >= ns) {
             if (!tail) return -1;
-            xhat[o] = (double)kvqo_f16_to_f32(tail[(((long)b * heads + h) * group + (t - ns)) * dim + c]);
+            xhat[o] = (double)kvqo_f16_to_f32(tail[(((long)b * heads + h) * rows + (t - ns)) * dim + c]);
             continue;
           }
           long mi;
@@ -374,12 +406,12 @@ int kvqo_attention(const double* khat, const double* vhat, const float* q, const
  * fp16 tail (2 bytes per unsealed element).  out[0..2] = packed, meta, tail.
  * Packed bytes are counted exactly: elements*bits/8 (rounded up per tensor). */
 void kvqo_tensor_bytes(int batch, int heads, int dim, const int* lens, int bits, int group, int axis, int sym,
-                       int meta_f32, double* out) {
+                       int meta_f32, int window, double* out) {
   double packed_bits = 0.0, meta = 0.0, tail = 0.0;
   double per_group = (sym ? 2.0 : 4.0) * (meta_f32 ? 2.0 : 1.0);
   for (int b = 0; b < batch; ++b) {
     long n = lens[b];
-    long ns = kvqo_sealed(n, axis, group);
+    long ns = kvqo_sealed(n, axis, group, window);
     packed_bits += (double)ns * heads * dim * bits;
     tail += (double)(n - ns) * heads * dim * 2.0;
     if (axis == KVQO_PER_CHANNEL) meta += (double)(ns / group) * heads * dim * per_group;

@@ -263,3 +263,80 @@ def test_per_channel_groups_use_the_fp16_staging_values():
     mp = pre["meta"].reshape(1, 2, 3, 64, 2)
     ma = a["meta"].reshape(1, 2, 3, 64, 2)
     np.testing.assert_array_equal(mp[:, :, :2], ma[:, :, :2])
+
+
+# ---------------------------------------------------------------------------
+# Full-precision recent window ("O Seu Cache KV Nao Tem um Problema de Bits...",
+# section "O Imposto dos Sistemas e Por Que Nao E um Detalhe": the newest
+# tokens, up to 128, stay in full precision; groups are quantized once enough
+# tokens have accumulated).  Reading: per-channel groups seal once all their
+# tokens are older than the newest R; per-token tensors quantize 16-token
+# blocks once all of the block is older than the newest R; tokens quantized
+# after a stay in the window are quantized from their fp16 values.
+
+@pytest.mark.parametrize("n,axis,group,window,expect", [
+    (100, oracle.PER_CHANNEL, 32, 64, 32), (96, oracle.PER_CHANNEL, 32, 64, 32), (95, oracle.PER_CHANNEL, 32, 64, 0),
+    (100, oracle.PER_CHANNEL, 32, 0, 96), (100, oracle.PER_TOKEN, 32, 32, 64), (47, oracle.PER_TOKEN, 32, 32, 0),
+    (48, oracle.PER_TOKEN, 32, 32, 16), (100, oracle.PER_TOKEN, 32, 0, 100), (10, oracle.PER_TOKEN, 32, 128, 0)])
+def test_window_sealed_counts(n, axis, group, window, expect):
+    assert oracle.sealed(n, axis, group, window) == expect
+    assert oracle.tail_rows(axis, group, window) == (group + window if axis == oracle.PER_CHANNEL
+                                                     else (window + 16 if window else 0))
+
+
+def _fp16_round(x):
+    return np.asarray(x, np.float32).astype(np.float16).astype(np.float32)
+
+
+@pytest.mark.parametrize("axis,group", [(oracle.PER_TOKEN, 32), (oracle.PER_TOKEN, oracle.WHOLE_VECTOR),
+                                        (oracle.PER_CHANNEL, 32), (oracle.PER_CHANNEL, 16)])
+@pytest.mark.parametrize("window", [16, 64])
+def test_window_keeps_recent_tokens_in_fp16(axis, group, window):
+    rng = np.random.default_rng(7)
+    B, T, H, D = 2, 150, 2, 64
+    x = rng.standard_normal((B, T, H, D)).astype(np.float32)
+    lens = [150, 77]
+    tcap = 160
+    q = oracle.quantize_tensor(x, lens, tcap, 4, group, axis, window=window)
+    q0 = oracle.quantize_tensor(_fp16_round(x), lens, tcap, 4, group, axis, window=0)
+    g = oracle.resolve_group(group, H, D)
+    xh = oracle.dequant_tensor(q, lens, 4, group, axis, window=window)
+    xh0 = oracle.dequant_tensor(q0, lens, 4, group, axis, window=0)
+    for b, n in enumerate(lens):
+        ns = oracle.sealed(n, axis, g, window)
+        assert n - ns >= (window if n >= window else n)  # at least the newest R tokens stay fp16
+        # window rows: the input rounded to nearest fp16, row t - sealed
+        rows = q["tail"][b, :, : n - ns].view(np.float16).astype(np.float32)
+        np.testing.assert_array_equal(rows, _fp16_round(x[b, ns:n]).transpose(1, 0, 2))
+        np.testing.assert_array_equal(xh[b, :, ns:n], _fp16_round(x[b, ns:n]).transpose(1, 0, 2).astype(np.float64))
+        # no codes past the sealed prefix
+        assert not q["codes"][b, :, ns:].any()
+        # the sealed prefix is what quantizing the fp16 values without a window gives
+        np.testing.assert_array_equal(q["codes"][b, :, :ns], q0["codes"][b, :, :ns])
+        np.testing.assert_array_equal(xh[b, :, :ns], xh0[b, :, :ns])
+
+
+@pytest.mark.parametrize("axis", [oracle.PER_TOKEN, oracle.PER_CHANNEL])
+def test_window_sealed_prefix_never_changes_as_tokens_arrive(axis):
+    """A token's codes, once sealed, are the same for every later length
+    (the window slides; nothing already quantized is requantized)."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, 200, 2, 64)).astype(np.float32)
+    prev = None
+    for n in range(60, 200, 7):
+        q = oracle.quantize_tensor(x, [n], 208, 3, 32, axis, window=48)
+        ns = oracle.sealed(n, axis, 32, 48)
+        if prev is not None:
+            pq, pns = prev
+            np.testing.assert_array_equal(q["codes"][0, :, :pns], pq["codes"][0, :, :pns])
+        prev = (q, ns)
+
+
+def test_window_byte_terms():
+    lens = [150, 77]
+    p, m, t = oracle.tensor_bytes(2, 3, 64, lens, 2, 32, oracle.PER_TOKEN, window=32)
+    ns = [oracle.sealed(n, oracle.PER_TOKEN, 32, 32) for n in lens]
+    assert ns == [112, 32]
+    assert t == sum(n - s for n, s in zip(lens, ns)) * 3 * 64 * 2
+    assert p == sum(ns) * 3 * 64 * 2 / 8
+    assert m == sum(ns) * 3 * (64 // 32) * 4
