@@ -35,7 +35,8 @@ bool valid_tensor(const kvq_tensor_cfg& t, int D, int H) {
 kvq_status validate(const kvq_config* c) {
   if (!c) return KVQ_ERR_INVALID_ARG;
   if (c->layers < 1 || c->batch < 1 || c->kv_heads < 1 || c->q_heads < 1 || c->max_tokens < 1 ||
-      c->max_splits < 0 || c->max_splits > kMaxSplits)
+      c->max_splits < 0 || c->max_splits > kMaxSplits || c->recent_window < 0 || c->recent_window % 16 ||
+      c->recent_window > 1024)
     return KVQ_ERR_INVALID_ARG;
   if (c->batch > kMaxBatch) return KVQ_ERR_UNSUPPORTED;
   if (c->q_heads % c->kv_heads) return KVQ_ERR_INVALID_ARG;
@@ -73,6 +74,8 @@ TensorLayout make_layout(const kvq_tensor_cfg& t, const kvq_config& c) {
   L.gpt = (t.axis == KVQ_PER_TOKEN) ? (L.whole ? 1 : c.head_dim / t.group) : 0;
   L.tile_words = c.head_dim * t.bits / 2;
   L.planes = planes_of(t.bits);
+  L.window = c.recent_window;
+  L.ring = t.axis == KVQ_PER_CHANNEL ? L.group + L.window : (L.window ? L.window + kTile : 0);
   return L;
 }
 
@@ -112,8 +115,8 @@ size_t carve(const kvq_config& c, kvq_cache* C) {
     T.meta_layer = align256((size_t)groups * T.meta_bytes);
     T.meta_off = off;
     off += T.meta_layer * L;
-    if (T.axis == 1) {
-      T.tail_layer = align256((size_t)B * H * T.group * D * 2);
+    if (T.ring) {
+      T.tail_layer = align256((size_t)B * H * T.ring * D * 2);
       T.tail_off = off;
       off += T.tail_layer * L;
     }
@@ -153,7 +156,7 @@ void tensor_terms(const TensorLayout& T, const kvq_config& c, const int32_t* len
   double pb = 0, m = 0, tl = 0;
   for (int b = 0; b < c.batch; ++b) {
     long n = lens[b];
-    long ns = T.axis == 1 ? (n / T.group) * T.group : n;
+    long ns = sealed_tokens(T, n);
     pb += (double)ns * H * D * T.bits;
     tl += (double)(n - ns) * H * D * 2.0;
     if (T.axis == 1) m += (double)(ns / T.group) * H * D * T.meta_bytes;

@@ -100,6 +100,8 @@ __host__ __device__ inline void plane_word_bit(const FragPos& f, int D, int w, i
 // Layout of one tensor (keys or values) of every layer inside the buffer.
 struct TensorLayout {
   int bits, group, axis, sym, whole;  // whole: per-token group spanning all kv heads
+  int window;                         // full-precision window of the newest tokens (0: none)
+  int ring;                           // fp16 rows per (sequence, head): token t at row t % ring (0: no fp16 rows)
   int meta_f32;
   int meta_bytes;       // bytes per stored group entry
   int gpt;              // per-token axis: groups per head row (D/G), 1 when whole
@@ -109,6 +111,18 @@ struct TensorLayout {
   size_t meta_off, meta_layer;
   size_t tail_off, tail_layer;    // per-channel only
 };
+
+// Tokens of a length-n sequence held as codes; the rest [sealed, n) are fp16
+// rows.  Per-channel: whole groups older than the window; per-token: every
+// token (no window) or whole 16-token blocks older than the window.
+__host__ __device__ inline long sealed_tokens(int axis, int group, int window, long n) {
+  const long old = n - window > 0 ? n - window : 0;
+  if (axis == 1) return (old / group) * group;
+  return window ? (old / 16) * 16 : n;
+}
+__host__ __device__ inline long sealed_tokens(const TensorLayout& L, long n) {
+  return sealed_tokens(L.axis, L.group, L.window, n);
+}
 
 // ------------------------------------------------------------- fp helpers --
 

@@ -52,6 +52,8 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
     d.meta_bytes = L.meta_bytes;
     d.tile_bytes = L.tile_words * 4;
     d.mtile_bytes = L.axis == 0 ? meta_tile_bytes(L) : D * L.meta_bytes;
+    d.window = L.window;
+    d.ring = L.ring;
   };
   fill(a.K, C->k);
   fill(a.V, C->v);
@@ -240,6 +242,8 @@ cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16,
     d.group = cfg.max_tokens;  // row stride of a (sequence, head)
     d.lg_group = 30;           // nothing is ever sealed
     d.gpt = 0;
+    d.window = 0;
+    d.ring = cfg.max_tokens;   // token t at row t
   };
   tail_only(a.K, k16);
   tail_only(a.V, v16);

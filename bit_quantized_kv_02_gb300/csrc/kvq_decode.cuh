@@ -423,8 +423,11 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int w0 = chunk * S + warp * a.Sw;
   const int w1 = min(w0 + a.Sw, n);
   const int ntl = w1 > w0 ? (w1 - w0 + kTile - 1) / kTile : 0;
-  const int sealed_k = k_token ? n : ((n >> k_lgG) << k_lgG);
-  const int sealed_v = VAXIS == 0 ? n : ((n >> v_lgG) << v_lgG);
+  // tokens held as codes; the newer ones are fp16 rows (unsealed per-channel
+  // groups and the full-precision window)
+  const int kold = max(n - a.K.window, 0), vold = max(n - a.V.window, 0);
+  const int sealed_k = k_token ? (a.K.window ? (kold >> 4) << 4 : n) : ((kold >> k_lgG) << k_lgG);
+  const int sealed_v = VAXIS == 0 ? (a.V.window ? (vold >> 4) << 4 : n) : ((vold >> v_lgG) << v_lgG);
   const long bh = (long)b * H + h;
   const char* kc_src = a.K.codes + (bh * ntiles + (w0 >> 4)) * (long)kc_bytes;
   const char* vc_src = a.V.codes + (bh * ntiles + (w0 >> 4)) * (long)vc_bytes;
@@ -433,8 +436,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
                                : a.K.meta + ((bh * (tcap >> k_lgG) + (w0 >> k_lgG)) * D) * kmb;
   const char* vm_src = VAXIS == 0 ? a.V.meta + (vwhole ? ((long)b * tcap + w0) : ((bh * tcap + w0) * vgpt)) * vmb
                                   : a.V.meta + ((bh * (tcap >> v_lgG) + (w0 >> v_lgG)) * D) * vmb;
-  const __half* ktail = a.K.tail + bh * kG * D;
-  const __half* vtail = a.V.tail + bh * vG * D;
+  const int kring = a.K.ring, vring = a.V.ring;
+  const __half* ktail = a.K.tail + bh * kring * D;
+  const __half* vtail = a.V.tail + bh * vring * D;
   const int kgmask = k_token ? 0 : kG - 1;
   const int vgmask = VAXIS == 0 ? 0 : vG - 1;
 
@@ -547,7 +551,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int E_unit = norm_exp(qmax);
   const int E_chan = k_token ? E_unit : norm_exp(qmax * smax_k);
   int Ek = E_unit;
-  bool qb_unit = false;
+  int qb_state = -1;  // query operand held: 0 unit with the key conversion's column scale, 1 plain unit, 2 key group
   // conversion exponents of the key and value codes (A = 2^(g + r*rowhalf +
   // c*colhalf) * (code + off)): key columns are channels (compensated in the
   // query operand), key rows tokens (in the score fold); value rows are
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const float v_chi = exp2i(-conv_c(vbits));
   if (k_token) {
     build_qb<D, R8>(qs, rep, nullptr, kbits, ksym, kf32, barea, wbias, E_unit, k_chi, lane);
-    qb_unit = true;
+    qb_state = 0;
     load_b();
   }
   // value step normalisation: every folded p * step lies below 2^15
@@ -588,6 +592,54 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int gc_grp = GC ? (g >> 1) % gs_v : 0;
   const int pv_rho = GC ? (g >> 1) / gs_v : (g >> 1);
 
+  // Per-token values: the packed tiles accumulate O in scaled units (2^E_v, the
+  // conversion's row exponent) with the zero points apart in Zs; before the
+  // first fp16 row of the window, O is turned into plain units (as the
+  // epilogue would) so that fp16 rows accumulate directly.
+  bool o_real = false;
+  auto to_real = [&]() {
+#pragma unroll
+    for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
+#pragma unroll
+      for (int q = 0; q < SL::N; ++q) {
+        float v = Zs[jg][q];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        Zs[jg][q] = v;
+      }
+    const int lg_gsz = vwhole ? 30 : v_lgG;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int c = 16 * j + g + 8 * rr, jg = c >> lg_gsz;
+        float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+        for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u) {
+          const float zt = __shfl_sync(0xffffffffu, Zs[u][0] + Zs[u][1], min(tig / max(gs_v, 1), rep - 1));
+          if (u == jg) {
+            if (R8) {
+              z0 = Zs[u][0] + Zs[u][2];
+              z1 = Zs[u][1] + Zs[u][3];
+            } else if (GC) {
+              z0 = (tig % gs_v == jg) ? zt : 0.0f;
+            } else {
+              z0 = Zs[u][0] + Zs[u][1];
+            }
+          }
+        }
+        const float osc = inv_sc_v * exp2i(-v_cg - (rr ? v_cr : 0));
+        O[j][2 * rr] = O[j][2 * rr] * osc + z0;
+        O[j][2 * rr + 1] = O[j][2 * rr + 1] * osc + z1;
+      }
+    }
+#pragma unroll
+    for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
+#pragma unroll
+      for (int q = 0; q < SL::N; ++q) Zs[jg][q] = 0.0f;
+    o_real = true;
+  };
+
   // One 16-token tile.  FAST: the tile is full and both its keys and values are
   // packed (the bulk of every range), so the tail and partial-tile checks fold away.
   auto tile_body = [&](const int i, auto stag, auto ftag) {
@@ -606,20 +658,26 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     // ---- metadata of this stage -> canonical fp32 pairs
     if (kp) {
       if (k_token) {
+        if (qb_state != 0) {
+          Ek = E_unit;
+          build_qb<D, R8>(qs, rep, nullptr, kbits, ksym, kf32, barea, wbias, E_unit, k_chi, lane);
+          qb_state = 0;
+          load_b();
+        }
         canon_meta(reinterpret_cast<const char*>(st + st_km), kTile * gs_k, kbits, ksym, kf32, exp2i(-Ek - k_cg),
                    exp2i(-Ek - k_cg - k_cr), 8 * gs_k, canK, lane);
       } else if ((t0 & kgmask) == 0) {
         Ek = E_chan;
         build_qb<D, R8>(qs, rep, reinterpret_cast<const char*>(st + st_km), kbits, ksym, kf32, barea, wbias, E_chan,
                         k_chi, lane);
-        qb_unit = false;
+        qb_state = 2;
         load_b();
       }
-    } else if (!qb_unit) {
-      // fp16 tail of per-channel keys: plain operands, no conversion scale
+    } else if (qb_state != 1) {
+      // fp16 rows of the keys: plain operands, no conversion scale
       Ek = E_unit;
       build_qb<D, R8>(qs, rep, nullptr, kbits, ksym, kf32, barea, wbias, E_unit, 1.0f, lane);
-      qb_unit = true;
+      qb_state = 1;
       load_b();
     }
     if (vp) {
@@ -705,7 +763,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           // fp16 tail rows: token row R = g + 8*rh, channels 16j + 2tig + 8*kh (+1)
-          const __half* tb = ktail + (long)(t0 - sealed_k) * D + 16 * j + 2 * tig;
+          const __half* tb = ktail + (long)(t0 % kring) * D + 16 * j + 2 * tig;
           uint32_t A[4];
           A[0] = *reinterpret_cast<const uint32_t*>(tb + (long)g * D);
           A[1] = *reinterpret_cast<const uint32_t*>(tb + (long)(g + 8) * D);
@@ -888,11 +946,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           default: pv_packed(IntC<8>{}); break;
         }
       } else {
+        if (VAXIS == 0 && !o_real) to_real();  // per-token values: the packed part is complete
         make_b(pv[0], pv[1], pv[2], pv[3]);
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
-          // fp16 tail: rows = channels 16j + g (+8), columns = tokens 2tig (+1) (+8)
-          const __half* tb = vtail + (long)(t0 - sealed_v) * D + 16 * j + g;
+          // fp16 rows: rows = channels 16j + g (+8), columns = tokens 2tig (+1) (+8)
+          const __half* tb = vtail + (long)(t0 % vring) * D + 16 * j + g;
           auto pr = [&](int t, int coff) -> uint32_t {
             return pack_h2(tb[(long)t * D + coff], tb[(long)(t + 1) * D + coff]);
           };
@@ -1028,7 +1087,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           rho0 = 2 * tig;
           rho1 = 2 * tig + 1;
         }
-        if (VAXIS == 0) {
+        if (VAXIS == 0 && !o_real) {
           const int jg = c >> lg_gsz;
           float z0 = 0.f, z1 = 0.f;
 #pragma unroll

@@ -18,6 +18,8 @@ struct DecTensor {
   int meta_bytes;       // bytes of one stored entry
   int tile_bytes;       // packed bytes of one 16-token tile
   int mtile_bytes;      // per-token: metadata bytes per tile; per-channel: per group
+  int window;           // full-precision window of the newest tokens (0: none)
+  int ring;             // fp16 rows per (sequence, head): token t at row t % ring
 };
 
 struct DecodeArgs {

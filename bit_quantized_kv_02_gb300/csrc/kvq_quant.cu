@@ -143,9 +143,13 @@ __device__ __forceinline__ char* meta_ptr(const QuantArgs& a) {
   return a.base + a.L.meta_off + a.layer * a.L.meta_layer;
 }
 __device__ __forceinline__ long bh_of(const QuantArgs& a, int b, int h) { return (long)b * a.H + h; }
+// fp16 rows of (b, h): ring of L.ring rows, token t at row t % ring
 __device__ __forceinline__ __half* tail_ptr(const QuantArgs& a, int b, int h) {
   return reinterpret_cast<__half*>(a.base + a.L.tail_off + a.layer * a.L.tail_layer) +
-         (((long)b * a.H + h) * a.L.group) * a.D;
+         (((long)b * a.H + h) * a.L.ring) * a.D;
+}
+__device__ __forceinline__ __half* tail_row(const QuantArgs& a, int b, int h, long t) {
+  return tail_ptr(a, b, h) + (t % a.L.ring) * a.D;
 }
 
 // Quantize a per-channel group block: G tokens x D channels of head h held in
@@ -188,17 +192,17 @@ __global__ void prefill_channel_kernel(QuantArgs a) {
   const int g = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = a.L.group, D = a.D;
   const int n = a.lens[b];
-  const int ng = n / G;
-  if (g > ng || (g == ng && n % G == 0)) return;
+  const int ns = (int)sealed_tokens(a.L, n);
+  const int ng = ns / G;
+  if (g > ng || (g == ng && ns == n)) return;
   const long xs_t = (long)a.H * D;
   const char* xb = reinterpret_cast<const char*>(a.x);
-  if (g == ng) {  // tail: tokens [ng*G, n) rounded to nearest fp16
-    __half* tail = tail_ptr(a, b, h);
-    int cnt = (n - ng * G) * D;
+  if (g == ng) {  // unsealed tokens [ns, n) rounded to nearest fp16, into the fp16 rows
+    int cnt = (n - ns) * D;
     for (int i = threadIdx.x; i < cnt; i += blockDim.x) {
       int tt = i / D, c = i % D;
-      long src = ((long)b * a.t_stride + ng * G + tt) * xs_t + (long)h * D + c;
-      tail[(long)tt * D + c] = __float2half_rn(load_in(xb, src, a.x_f32));
+      long src = ((long)b * a.t_stride + ns + tt) * xs_t + (long)h * D + c;
+      tail_row(a, b, h, ns + tt)[c] = __float2half_rn(load_in(xb, src, a.x_f32));
     }
     return;
   }
@@ -216,37 +220,23 @@ __global__ void prefill_channel_kernel(QuantArgs a) {
   quant_channel_block(a, b, h, g, xs, cs, zs, ss);
 }
 
-// Per-token tensors: one CTA per (tile, head, sequence); for whole-vector
-// groups one CTA per (tile, sequence) covering every head (blockIdx.y == 0).
-__global__ void prefill_token_kernel(QuantArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int tile = blockIdx.x, b = blockIdx.z;
-  const int D = a.D;
-  const int n = a.lens[b];
-  if (tile * kTile >= n) return;
-  const int whole = a.L.whole;
-  const int h0 = whole ? 0 : blockIdx.y, nh = whole ? a.H : 1;
-  const int rowlen = nh * D;  // channels handled per token
+// Quantize one 16-token tile of a per-token tensor: tokens tile*16 + tt (tt <
+// valid) of heads h0 .. h0+nh-1 held in shared memory as floats xs[16][nh*D];
+// writes each token's group metadata and the nh packed tiles.  All threads of
+// the block participate.
+__device__ void quant_token_tile(const QuantArgs& a, int b, int h0, int nh, int tile, int valid, const float* xs,
+                                 uint8_t* cs, float* zs, float* ss) {
+  const int D = a.D, whole = a.L.whole;
+  const int rowlen = nh * D;
   const int G = whole ? rowlen : a.L.group;
   const int gpr = rowlen / G;  // groups per token row in this CTA
-  float* xs = reinterpret_cast<float*>(smem);                       // [16][rowlen]
-  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kTile * rowlen);    // [nh][16][D]
-  float* zs = reinterpret_cast<float*>(cs + kTile * rowlen);        // [16*gpr]
-  float* ss = zs + kTile * gpr;
-  const long xs_t = (long)a.H * D;
-  for (int i = threadIdx.x; i < kTile * rowlen; i += blockDim.x) {
-    int tt = i / rowlen, c = i % rowlen;
-    int t = tile * kTile + tt;
-    xs[i] = t < n ? load_in(a.x, ((long)b * a.t_stride + t) * xs_t + (long)h0 * D + c, a.x_f32) : 0.0f;
-  }
-  __syncthreads();
   const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   char* meta = meta_ptr(a);
   float smax_local = 0.0f;
   for (int gi = warp; gi < kTile * gpr; gi += nwarp) {
     int tt = gi / gpr, j = gi % gpr;
     int t = tile * kTile + tt;
-    if (t >= n) continue;
+    if (tt >= valid) continue;
     float mn, mx, am;
     warp_stats(xs + tt * rowlen + j * G, G, 1, &mn, &mx, &am);
     float z, s;
@@ -262,16 +252,57 @@ __global__ void prefill_token_kernel(QuantArgs a) {
   __syncthreads();
   for (int i = threadIdx.x; i < kTile * rowlen; i += blockDim.x) {
     int tt = i / rowlen, c = i % rowlen;
-    int t = tile * kTile + tt;
     int hh = c / D, cc = c % D;
     uint8_t code = 0;
-    if (t < n) code = (uint8_t)quant_code(xs[i], zs[tt * gpr + c / G], ss[tt * gpr + c / G], a.L.bits, a.L.sym);
+    if (tt < valid) code = (uint8_t)quant_code(xs[i], zs[tt * gpr + c / G], ss[tt * gpr + c / G], a.L.bits, a.L.sym);
     cs[(hh * kTile + tt) * D + cc] = code;
   }
   __syncthreads();
   for (int hh = 0; hh < nh; ++hh) store_tile(codes_ptr(a, b, h0 + hh, tile), cs + hh * kTile * D, D, a.L, a.is_value);
   if ((threadIdx.x & 31) == 0 && smax_local > 0.0f)
     for (int hh = 0; hh < nh; ++hh) atomic_max_pos(a.smax + (long)b * a.H + h0 + hh, smax_local);
+}
+
+// Per-token tensors: one CTA per (tile, head, sequence); for whole-vector
+// groups one CTA per (tile, sequence) covering every head (blockIdx.y == 0).
+// With a recent window, tiles older than the window are quantized from the
+// inputs rounded to fp16 and the newer tiles go to the fp16 rows.
+__global__ void prefill_token_kernel(QuantArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tile = blockIdx.x, b = blockIdx.z;
+  const int D = a.D;
+  const int n = a.lens[b];
+  if (tile * kTile >= n) return;
+  const int ns = (int)sealed_tokens(a.L, n);
+  const int whole = a.L.whole;
+  const int h0 = whole ? 0 : blockIdx.y, nh = whole ? a.H : 1;
+  const int rowlen = nh * D;  // channels handled per token
+  const int G = whole ? rowlen : a.L.group;
+  const int gpr = rowlen / G;
+  const long xs_t = (long)a.H * D;
+  if (tile * kTile >= ns) {  // fp16 rows (a window's tiles are never partly sealed)
+    for (int i = threadIdx.x; i < kTile * rowlen; i += blockDim.x) {
+      int tt = i / rowlen, c = i % rowlen;
+      int t = tile * kTile + tt;
+      if (t >= n) continue;
+      tail_row(a, b, h0 + c / D, t)[c % D] =
+          __float2half_rn(load_in(a.x, ((long)b * a.t_stride + t) * xs_t + (long)h0 * D + c, a.x_f32));
+    }
+    return;
+  }
+  float* xs = reinterpret_cast<float*>(smem);                       // [16][rowlen]
+  uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kTile * rowlen);    // [nh][16][D]
+  float* zs = reinterpret_cast<float*>(cs + kTile * rowlen);        // [16*gpr]
+  float* ss = zs + kTile * gpr;
+  for (int i = threadIdx.x; i < kTile * rowlen; i += blockDim.x) {
+    int tt = i / rowlen, c = i % rowlen;
+    int t = tile * kTile + tt;
+    float x = t < n ? load_in(a.x, ((long)b * a.t_stride + t) * xs_t + (long)h0 * D + c, a.x_f32) : 0.0f;
+    if (a.L.window) x = __half2float(__float2half_rn(x));  // quantized after a stay in the window
+    xs[i] = x;
+  }
+  __syncthreads();
+  quant_token_tile(a, b, h0, nh, tile, min(kTile, n - tile * kTile), xs, cs, zs, ss);
 }
 
 // lens[b] and every per-head copy head_lens[b][h] of the layer
@@ -302,16 +333,26 @@ __device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, 
   const int lane = threadIdx.x & 31;
   const int D = a.D;
   const long xs_t = (long)a.H * D;
+  const int R = a.L.window;
   if (a.L.axis == 1) {
+    // fp16 row; a group seals once all its tokens are older than the window
     const int G = a.L.group;
-    const int slot = n & (G - 1);
-    __half* tail = tail_ptr(a, b, h) + (long)slot * D;
-    for (int c = lane; c < D; c += 32) tail[c] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
-    return slot == G - 1;
+    __half* row = tail_row(a, b, h, n);
+    for (int c = lane; c < D; c += 32) row[c] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
+    const int old = n + 1 - R;
+    return old >= G && old % G == 0;
   }
   const int whole = a.L.whole;
   const int nh = whole ? a.H : 1;
   const int rowlen = nh * D;
+  if (R) {
+    // per-token tensor with a window: fp16 row now, its 16-token block is
+    // quantized once all of it is older than the window
+    for (int c = lane; c < rowlen; c += 32)
+      tail_row(a, b, h + c / D, n)[c % D] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
+    const int old = n + 1 - R;
+    return old >= kTile && old % kTile == 0;
+  }
   const int G = whole ? rowlen : a.L.group;
   const int gpr = rowlen / G;
   for (int c = lane; c < rowlen; c += 32) xs[c] = load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32);
@@ -413,15 +454,34 @@ __global__ void append_kernel(const __grid_constant__ AppendArgs a) {
   for (int w = 0; w < 2; ++w) {
     if (!seal[w]) continue;
     const QuantArgs& q = w == 0 ? a.k : a.v;
-    const int G = q.L.group, D = q.D;
-    float* xs = reinterpret_cast<float*>(smem);
-    uint8_t* cs = reinterpret_cast<uint8_t*>(xs + G * D);
-    float* zs = reinterpret_cast<float*>(cs + G * D);
-    float* ss = zs + D;
-    const __half* tail = tail_ptr(q, b, h);
-    for (int i = threadIdx.x; i < G * D; i += blockDim.x) xs[i] = __half2float(tail[i]);
-    __syncthreads();
-    quant_channel_block(q, b, h, n / G, xs, cs, zs, ss);
+    const int D = q.D, old = n + 1 - q.L.window;
+    if (q.L.axis == 1) {
+      // seal per-channel group g from its fp16 rows
+      const int G = q.L.group, g = old / G - 1;
+      float* xs = reinterpret_cast<float*>(smem);
+      uint8_t* cs = reinterpret_cast<uint8_t*>(xs + G * D);
+      float* zs = reinterpret_cast<float*>(cs + G * D);
+      float* ss = zs + D;
+      for (int i = threadIdx.x; i < G * D; i += blockDim.x)
+        xs[i] = __half2float(tail_row(q, b, h, (long)g * G + i / D)[i % D]);
+      __syncthreads();
+      quant_channel_block(q, b, h, g, xs, cs, zs, ss);
+    } else {
+      // quantize per-token block `tile` from its fp16 rows (all heads for whole-vector groups)
+      const int tile = old / kTile - 1;
+      const int nh = q.L.whole ? q.H : 1, rowlen = nh * D;
+      const int gpr = rowlen / (q.L.whole ? rowlen : q.L.group);
+      float* xs = reinterpret_cast<float*>(smem);                     // [16][rowlen]
+      uint8_t* cs = reinterpret_cast<uint8_t*>(xs + kTile * rowlen);  // [nh][16][D]
+      float* zs = reinterpret_cast<float*>(cs + kTile * rowlen);
+      float* ss = zs + kTile * gpr;
+      for (int i = threadIdx.x; i < kTile * rowlen; i += blockDim.x) {
+        const int tt = i / rowlen, c = i % rowlen;
+        xs[i] = __half2float(tail_row(q, b, h + c / D, (long)tile * kTile + tt)[c % D]);
+      }
+      __syncthreads();
+      quant_token_tile(q, b, h, nh, tile, kTile, xs, cs, zs, ss);
+    }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
@@ -439,10 +499,7 @@ struct ExportArgs {
   uint16_t* tail;    // [B][H][G][D] or null
 };
 
-__device__ __forceinline__ int sealed_of(const TensorLayout& L, int n) {
-  return L.axis == 1 ? (n / L.group) * L.group : n;
-}
-
+__device__ __forceinline__ int sealed_of(const TensorLayout& L, int n) { return (int)sealed_tokens(L, n); }
 // codes: one CTA per (tile, head, sequence)
 __global__ void export_codes_kernel(ExportArgs e) {
   const QuantArgs& a = e.a;
@@ -475,15 +532,15 @@ __global__ void export_meta_kernel(ExportArgs e, long ngroups) {
     long per_b = (long)a.H * (a.tcap / a.L.group) * D;
     b = (int)(gi / per_b);
     long g = (gi / D) % (a.tcap / a.L.group);
-    valid = g < a.lens[b] / a.L.group;
+    valid = g < sealed_of(a.L, a.lens[b]) / a.L.group;
   } else if (a.L.whole) {
     b = (int)(gi / a.tcap);
-    valid = (gi % a.tcap) < a.lens[b];
+    valid = (gi % a.tcap) < sealed_of(a.L, a.lens[b]);
   } else {
     long per_b = (long)a.H * a.tcap * a.L.gpt;
     b = (int)(gi / per_b);
     long t = (gi / a.L.gpt) % a.tcap;
-    valid = t < a.lens[b];
+    valid = t < sealed_of(a.L, a.lens[b]);
   }
   float z = 0.0f, s = 0.0f;
   if (valid) load_meta(meta_ptr(a), gi, a.L.meta_f32, a.L.sym, &z, &s);
@@ -491,15 +548,15 @@ __global__ void export_meta_kernel(ExportArgs e, long ngroups) {
   e.meta[2 * gi + 1] = s;
 }
 
-// tail: one CTA per (head, sequence)
+// fp16 rows in token order (row t - sealed): one CTA per (head, sequence)
 __global__ void export_tail_kernel(ExportArgs e) {
   const QuantArgs& a = e.a;
-  const int h = blockIdx.y, b = blockIdx.z, D = a.D, G = a.L.group;
-  const int n = a.lens[b], cnt = n - (n / G) * G;
-  const __half* src = tail_ptr(a, b, h);
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
-    uint16_t v = (i / D) < cnt ? __half_as_ushort(src[i]) : (uint16_t)0;
-    e.tail[(((long)b * a.H + h) * G) * D + i] = v;
+  const int h = blockIdx.y, b = blockIdx.z, D = a.D, rows = a.L.ring;
+  const int n = a.lens[b], ns = sealed_of(a.L, n);
+  for (int i = threadIdx.x; i < rows * D; i += blockDim.x) {
+    const int r = i / D, c = i % D;
+    uint16_t v = ns + r < n ? __half_as_ushort(tail_row(a, b, h, ns + r)[c]) : (uint16_t)0;
+    e.tail[(((long)b * a.H + h) * rows) * D + i] = v;
   }
 }
 
@@ -587,7 +644,7 @@ __global__ void __launch_bounds__(128) dequant_kernel(QuantArgs a, __half* out, 
     const int t = (i * 8) / D, c = (i * 8) % D, ta = t_base + t;
     if (ta >= n) continue;
     const uint4 v = ta < ns ? *reinterpret_cast<const uint4*>(to + t * D + c)
-                            : *reinterpret_cast<const uint4*>(tail_ptr(a, b, h) + (long)(ta - ns) * D + c);
+                            : *reinterpret_cast<const uint4*>(tail_row(a, b, h, ta) + c);
     *reinterpret_cast<uint4*>(dst + (long)t * D + c) = v;
   }
 }
@@ -664,8 +721,10 @@ static int append_warp_smem(const kvq_cache* C) {
 size_t append_smem(const kvq_cache* C) {
   size_t m = 2 * (size_t)append_warp_smem(C);
   const TensorLayout* ls[2] = {&C->k, &C->v};
-  for (int i = 0; i < 2; ++i)
+  for (int i = 0; i < 2; ++i) {
     if (ls[i]->axis == 1) m = std::max(m, channel_smem(ls[i]->group, C->cfg.head_dim));
+    else if (ls[i]->window) m = std::max(m, token_smem(C, *ls[i]));  // per-token block seal
+  }
   return m;
 }
 
@@ -742,7 +801,7 @@ cudaError_t launch_export(kvq_cache* C, int layer, int is_value, uint8_t* codes,
     long ng = meta_groups(C, e.a.L);
     export_meta_kernel<<<(unsigned)((ng + 255) / 256), 256, 0, st>>>(e, ng);
   }
-  if (tail && e.a.L.axis == 1) export_tail_kernel<<<dim3(1, H, B), 256, 0, st>>>(e);
+  if (tail && e.a.L.ring) export_tail_kernel<<<dim3(1, H, B), 256, 0, st>>>(e);
   return cudaGetLastError();
 }
 

@@ -41,7 +41,8 @@ class TensorCfg(ctypes.Structure):
 class Config(ctypes.Structure):
     _fields_ = [("layers", ctypes.c_int), ("batch", ctypes.c_int), ("q_heads", ctypes.c_int),
                 ("kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
-                ("k", TensorCfg), ("v", TensorCfg), ("meta_dtype", ctypes.c_int), ("max_splits", ctypes.c_int)]
+                ("k", TensorCfg), ("v", TensorCfg), ("meta_dtype", ctypes.c_int), ("max_splits", ctypes.c_int),
+                ("recent_window", ctypes.c_int)]
 
 
 class Bytes(ctypes.Structure):
@@ -105,13 +106,16 @@ def lib():
         return L
 
 
-def make_config(layers, batch, q_heads, kv_heads, head_dim, max_tokens, k, v, meta_dtype=F16, max_splits=0):
-    """k, v: (bits, group, axis, mode) tuples or dicts."""
+def make_config(layers, batch, q_heads, kv_heads, head_dim, max_tokens, k, v, meta_dtype=F16, max_splits=0,
+                recent_window=0):
+    """k, v: (bits, group, axis, mode) tuples or dicts; recent_window: fp16 window
+    of the newest tokens of both tensors (multiple of 16, 0 = none)."""
     def tc(t):
         if isinstance(t, dict):
             return TensorCfg(t["bits"], t["group"], t["axis"], t.get("mode", ASYM))
         return TensorCfg(*t)
-    return Config(layers, batch, q_heads, kv_heads, head_dim, max_tokens, tc(k), tc(v), meta_dtype, max_splits)
+    return Config(layers, batch, q_heads, kv_heads, head_dim, max_tokens, tc(k), tc(v), meta_dtype, max_splits,
+                  recent_window)
 
 
 def _check(st: int, what: str, handle=None):
@@ -254,15 +258,18 @@ class KVQCache:
                 return B * T
             return B * H * T * (D // t.group)
 
+        def rows(t):  # fp16 rows per (sequence, head): the unsealed tokens, row t - sealed
+            if t.axis == PER_CHANNEL:
+                return t.group + c.recent_window
+            return c.recent_window + 16 if c.recent_window else 0
+
         out = {
             "codes_k": torch.zeros((B, H, T, D), dtype=torch.uint8, device=dev),
             "codes_v": torch.zeros((B, H, T, D), dtype=torch.uint8, device=dev),
             "meta_k": torch.zeros((groups(c.k), 2), dtype=torch.float32, device=dev),
             "meta_v": torch.zeros((groups(c.v), 2), dtype=torch.float32, device=dev),
-            "tail_k": torch.zeros((B, H, c.k.group, D), dtype=torch.int16, device=dev)
-            if c.k.axis == PER_CHANNEL else None,
-            "tail_v": torch.zeros((B, H, c.v.group, D), dtype=torch.int16, device=dev)
-            if c.v.axis == PER_CHANNEL else None,
+            "tail_k": torch.zeros((B, H, rows(c.k), D), dtype=torch.int16, device=dev) if rows(c.k) else None,
+            "tail_v": torch.zeros((B, H, rows(c.v), D), dtype=torch.int16, device=dev) if rows(c.v) else None,
             "lens": torch.zeros((B,), dtype=torch.int32, device=dev),
         }
         _check(lib().kvq_export(self.handle, layer, _ptr(out["codes_k"]), _ptr(out["codes_v"]), _ptr(out["meta_k"]),

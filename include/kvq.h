@@ -90,6 +90,14 @@ typedef struct {
   int meta_dtype;  /* kvq_dtype of the stored zero point / step: KVQ_F16 (default) or KVQ_F32 */
   int max_splits;  /* split-K partitions per sequence for decode, <= 1024; 0 = default (about
                       4864 / (batch * kv_heads), at least 8, at most one per 64 tokens) */
+  int recent_window; /* full-precision window R of the newest tokens of both tensors, a multiple of 16,
+                        0..1024; 0 = none ("O Seu Cache KV Nao Tem um Problema de Bits...", section "O
+                        Imposto dos Sistemas e Por Que Nao E um Detalhe": the newest tokens, up to 128,
+                        stay in full precision and are quantized in groups once enough accumulate).  With
+                        R > 0 a per-channel group is sealed once all its tokens are older than the newest
+                        R, a per-token tensor quantizes a 16-token block once all of it is older than the
+                        newest R (from the tokens' fp16 values); the newer tokens are held in fp16.  With
+                        R = 0 per-token tensors quantize every token on arrival. */
 } kvq_config;
 
 /* Byte accounting.  The first four terms follow the memory model total =
@@ -181,7 +189,10 @@ kvq_status kvq_decode_attn_static(kvq_cache_t cache, int layer, const void* q, i
  *   meta_k/v  : float  [groups][2] = (zero, step) as stored (zero = 0 when
  *               symmetric); group order: per channel ((b*H+h)*(tcap/G)+t/G)*D+c,
  *               per token ((b*H+h)*tcap+t)*(D/G)+c/G, whole vector b*tcap+t;
- *   tail_k/v  : uint16 [batch][kv_heads][G][head_dim] fp16 bits (per-channel only);
+ *   tail_k/v  : uint16 [batch][kv_heads][rows][head_dim] fp16 bits of the
+ *               tokens held in fp16 (row t - sealed); rows = G + recent_window
+ *               for a per-channel tensor, recent_window + 16 for a per-token
+ *               tensor with a window; null / unused when a tensor has none;
  *   lens      : int32  [batch].
  * tcap is kvq_cache_tcap(). */
 kvq_status kvq_export(kvq_cache_t cache, int layer, uint8_t* codes_k, uint8_t* codes_v, float* meta_k,

@@ -45,7 +45,8 @@ def _cfg(**kw):
                 k=(4, 32, kvq.PER_CHANNEL, kvq.ASYM), v=(4, 32, kvq.PER_TOKEN, kvq.ASYM))
     base.update(kw)
     return kvq.make_config(base["layers"], base["batch"], base["q_heads"], base["kv_heads"], base["head_dim"],
-                           base["max_tokens"], base["k"], base["v"], base.get("meta_dtype", 0), base.get("max_splits", 0))
+                           base["max_tokens"], base["k"], base["v"], base.get("meta_dtype", 0), base.get("max_splits", 0),
+                           base.get("recent_window", 0))
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -54,6 +55,7 @@ def _cfg(**kw):
     (dict(v=(4, 48, 0, 0)), 2), (dict(v=(4, 128, 0, 0)), 2), (dict(k=(4, -1, 1, 0)), 1),
     (dict(k=(4, 32, 2, 0)), 1), (dict(k=(4, 32, 1, 5)), 1), (dict(meta_dtype=3), 1), (dict(layers=0), 1),
     (dict(kv_heads=16, head_dim=256, v=(4, -1, 0, 0), q_heads=16), 2),
+    (dict(recent_window=8), 1), (dict(recent_window=-16), 1), (dict(recent_window=1040), 1),
 ])
 def test_config_validation(L, kw, status):
     with pytest.raises(kvq.KVQError) as e:

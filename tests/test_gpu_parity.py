@@ -23,16 +23,16 @@ def _lib():
     kvq.lib()
 
 
-def make_cache(wl, max_tokens=None, max_splits=0, meta_dtype=kvq.F16):
+def make_cache(wl, max_tokens=None, max_splits=0, meta_dtype=kvq.F16, window=0):
     cfg = kvq.make_config(wl.layers, wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, max_tokens or wl.max_tokens,
-                          wl.k, wl.v, meta_dtype, max_splits)
+                          wl.k, wl.v, meta_dtype, max_splits, window)
     return kvq.KVQCache(cfg)
 
 
-def oracle_tensor(x_btHD, lens, tcap, tc, meta_f32):
+def oracle_tensor(x_btHD, lens, tcap, tc, meta_f32, window=0):
     bits, group, axis, mode = tc
     return oracle.quantize_tensor(x_btHD.float().numpy(), np.array(lens, np.int32), tcap, bits, group, axis,
-                                  bool(mode), bool(meta_f32))
+                                  bool(mode), bool(meta_f32), window)
 
 
 def assert_export_equal(exp, orq, tc, which):
@@ -40,7 +40,7 @@ def assert_export_equal(exp, orq, tc, which):
     meta = exp[f"meta_{which}"].cpu().numpy()
     np.testing.assert_array_equal(codes, orq["codes"], err_msg=f"codes_{which}")
     np.testing.assert_array_equal(meta.view(np.uint32), orq["meta"].view(np.uint32), err_msg=f"meta_{which}")
-    if tc[2] == kvq.PER_CHANNEL:
+    if orq["tail"] is not None:
         tail = exp[f"tail_{which}"].cpu().numpy().view(np.uint16)
         np.testing.assert_array_equal(tail, orq["tail"], err_msg=f"tail_{which}")
 
@@ -53,19 +53,21 @@ def rel_err_rows(out, ref):
     return d / np.maximum(r, 1e-30)
 
 
-def decode_ref(wl, orq_k, orq_v, lens, q_cpu, scale):
-    kh = oracle.dequant_tensor(orq_k, lens, wl.k[0], wl.k[1], wl.k[2], bool(wl.k[3]))
-    vh = oracle.dequant_tensor(orq_v, lens, wl.v[0], wl.v[1], wl.v[2], bool(wl.v[3]))
+def decode_ref(wl, orq_k, orq_v, lens, q_cpu, scale, window=0):
+    kh = oracle.dequant_tensor(orq_k, lens, wl.k[0], wl.k[1], wl.k[2], bool(wl.k[3]), window)
+    vh = oracle.dequant_tensor(orq_v, lens, wl.v[0], wl.v[1], wl.v[2], bool(wl.v[3]), window)
     return oracle.attention(kh, vh, q_cpu.float().numpy(), np.array(lens, np.int32), scale)
 
 
-def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0, generic=None, global_combine=False):
+def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0, generic=None, global_combine=False,
+             window=0):
     """Prefill `lens` tokens of layer `layer`, compare the export and the decode output.
     generic: None keeps the default kernel choice, True forces the generic kernel,
     False requires the compile-time specialisation.  global_combine: merge the
     split-K partials through the global workspace even when a cluster could."""
     T = max(max(lens), 1)
-    cache = make_cache(wl, max_tokens=T, max_splits=max_splits, meta_dtype=kvq.F32 if meta_f32 else kvq.F16)
+    cache = make_cache(wl, max_tokens=T, max_splits=max_splits, meta_dtype=kvq.F32 if meta_f32 else kvq.F16,
+                       window=window)
     if generic is True or global_combine:
         cache.kvq_set_decode_kernel((1 if generic else 0) | (2 if global_combine else 0))
     if generic is True:
@@ -77,8 +79,8 @@ def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0,
     cache.kvq_prefill_quantize(layer, k.cuda(), v.cuda(), lens_l)
     exp = cache.kvq_export(layer)
     torch.cuda.synchronize()
-    ok = oracle_tensor(k, lens_l, cache.tcap, wl.k, meta_f32)
-    ov = oracle_tensor(v, lens_l, cache.tcap, wl.v, meta_f32)
+    ok = oracle_tensor(k, lens_l, cache.tcap, wl.k, meta_f32, window)
+    ov = oracle_tensor(v, lens_l, cache.tcap, wl.v, meta_f32, window)
     assert_export_equal(exp, ok, wl.k, "k")
     assert_export_equal(exp, ov, wl.v, "v")
     assert exp["lens"].cpu().tolist() == lens_l
@@ -88,7 +90,7 @@ def run_case(wl, lens, meta_f32=False, check_decode=True, layer=0, max_splits=0,
         out = cache.kvq_decode_attn(layer, q.cuda(), scale=float(scale))
         torch.cuda.synchronize()
         assert cache.kvq_device_status() == 0
-        ref = decode_ref(wl, ok, ov, lens_l, q, scale)
+        ref = decode_ref(wl, ok, ov, lens_l, q, scale, window)
         err = rel_err_rows(out.cpu().numpy(), ref)
         for b, n in enumerate(lens_l):
             if n == 0:
@@ -288,3 +290,57 @@ def test_capacity_error_is_all_or_nothing():
     assert cache.kvq_get_lens(0) == [40, 10]
     for key in ("codes_k", "codes_v", "meta_k", "meta_v", "lens"):
         assert torch.equal(before[key], after[key])
+
+
+# Full-precision recent window ("O Seu Cache KV Nao Tem um Problema de Bits...",
+# section "O Imposto dos Sistemas e Por Que Nao E um Detalhe").
+WINDOW_CASES = [
+    ("w_mha64_k4pc_v4pt", 2, 4, 4, 64, (4, 32, PC, ASYM), (4, 32, PT, ASYM), [300, 77], 64),
+    ("w_mha128_kt_vt", 2, 2, 2, 128, (2, 32, PT, ASYM), (2, 32, PT, ASYM), [161, 40], 32),
+    ("w_gqa8_256_pt", 1, 16, 2, 256, (4, 32, PT, ASYM), (8, 32, PT, ASYM), [700], 128),
+    ("w_whole", 2, 4, 4, 64, (3, WHOLE, PT, ASYM), (3, WHOLE, PT, ASYM), [65, 140], 16),
+    ("w_mha128_kc_vc", 1, 3, 3, 128, (2, 32, PC, ASYM), (2, 32, PC, ASYM), [1000], 128),
+    ("w_gqa2_sym", 2, 4, 2, 128, (4, 64, PC, SYM), (4, 64, PT, SYM), [500, 3], 48),
+]
+
+
+@pytest.mark.parametrize("generic", [None, True], ids=["default", "generic"])
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[c[0] for c in WINDOW_CASES])
+def test_window_parity(case, generic):
+    name, B, Hq, H, D, kc, vc, lens, window = case
+    wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=17)
+    run_case(wl, lens, generic=generic, window=window)
+
+
+@pytest.mark.parametrize("kc,vc,window", [((4, 32, PC, ASYM), (4, 32, PT, ASYM), 32),
+                                          ((2, 16, PC, SYM), (3, 32, PT, ASYM), 64),
+                                          ((5, 64, PT, ASYM), (6, WHOLE, PT, ASYM), 16)])
+def test_window_append_equals_prefill(kc, vc, window):
+    """Appending tokens one by one through a sliding window (fp16 rows, then
+    group / block sealing from them) gives bit-exactly the cache a prefill of
+    the same tokens gives, and the oracle's."""
+    wl = W("wapp", 2, 4, 2, 64, kc, vc, torch.float32, seed=19)
+    n0, steps = 20, 110
+    T = n0 + steps
+    k, v = wl.layer_kv(0, "cpu", T=T)
+    cache = make_cache(wl, max_tokens=T, window=window)
+    cache.kvq_prefill_quantize(0, k[:, :n0].contiguous().cuda(), v[:, :n0].contiguous().cuda(), [n0, n0])
+    for s in range(steps):
+        cache.kvq_append(0, k[:, n0 + s].contiguous().cuda(), v[:, n0 + s].contiguous().cuda())
+    exp = cache.kvq_export(0)
+    ref = make_cache(wl, max_tokens=T, window=window)
+    ref.kvq_prefill_quantize(0, k.cuda(), v.cuda(), [T, T])
+    exp2 = ref.kvq_export(0)
+    torch.cuda.synchronize()
+    for key in ("codes_k", "codes_v", "meta_k", "meta_v", "lens", "tail_k", "tail_v"):
+        if exp[key] is not None:
+            assert torch.equal(exp[key], exp2[key]), key
+    ok = oracle_tensor(k, [T, T], cache.tcap, wl.k, False, window)
+    ov = oracle_tensor(v, [T, T], cache.tcap, wl.v, False, window)
+    assert_export_equal(exp, ok, wl.k, "k")
+    assert_export_equal(exp, ov, wl.v, "v")
+    q = wl.layer_query(0)
+    scale = np.float32(0.125)
+    out = cache.kvq_decode_attn(0, q.cuda(), scale=float(scale))
+    ref_out = decode_ref(wl, ok, ov, [T, T], q, scale, window)
+    assert rel_err_rows(out.cpu().numpy(), ref_out).max() <= TOL
