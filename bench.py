@@ -228,7 +228,7 @@ def run_ours(args, rank, world):
     steps, warm = args.steps, args.warmup
     e2e_steps = min(steps, max(3, steps // 2))
     cap = wl.max_tokens + warm + steps + e2e_steps + 2
-    cfg = kvq.make_config(L, B, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v)
+    cfg = kvq.make_config(L, B, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v, recent_window=args.window)
     cache = kvq.KVQCache(cfg, device=dev)
     cache.kvq_set_decode_plan(cap)
     # prefill every layer from GPU-generated synthetic data (layer by layer)
@@ -330,7 +330,7 @@ def run_ours(args, rank, world):
     # then decode attention over those rows; timed like the fused decode graph
     mat = None
     if args.materialized:
-        shape = (B, H, cap, D)
+        shape = (B, H, cache.tcap, D)
         k16 = torch.zeros(shape, dtype=torch.float16, device=dev)
         v16 = torch.zeros(shape, dtype=torch.float16, device=dev)
         out_m = torch.empty_like(out)
@@ -387,14 +387,15 @@ def run_ours(args, rank, world):
             "vs_baseline": None, "dtype": "fp16 in, 2..8-bit codes, fp32 accumulate", "data": "synthetic",
             "pct_of_peak": round(100.0 * value / peak, 2),
             "cached_tokens_per_s": round(tokens_all / (t_max * 1e-3), 1),
-            "config": {"workload": wl.name, "layers": L, "batch_per_gpu": B, "q_heads": Hq, "kv_heads": H,
+            "config": {"workload": wl.name + (f"_w{args.window}" if args.window else ""), "layers": L,
+                       "batch_per_gpu": B, "q_heads": Hq, "kv_heads": H, "recent_window": args.window,
                        "head_dim": D, "cached_tokens": wl.lens[0], "k": list(wl.k), "v": list(wl.v),
                        "k_format": "bits,group,axis(0 per-token,1 per-channel),mode(0 asym,1 sym)",
                        "step": "per layer: kvq_append + kvq_decode_attn (CUDA graph)",
                        "l2": "256 MB buffer written before every timed step (L2 flushed)",
                        "parallelism": f"dp{world} (sequences sharded, no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload) if not args.tokens else None,
+                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload) if not (args.tokens or args.window) else None,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback",
                          "kernel": "decode_kernel", "bytes_per_launch": round(dec_bytes_per_launch),
@@ -456,6 +457,8 @@ def main():
     ap.add_argument("--workload", default="gpt2_small")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--tokens", type=int, default=0, help="cap the cached tokens per sequence (profiling runs)")
+    ap.add_argument("--window", type=int, default=0,
+                    help="full-precision recent window of both tensors (multiple of 16; 0 = none)")
     ap.add_argument("--materialized", action="store_true",
                     help="also time the materialised baseline (dequantize to fp16, then decode) beside the fused path")
     args = ap.parse_args()

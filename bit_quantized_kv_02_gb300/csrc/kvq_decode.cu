@@ -71,8 +71,11 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   a.gwork = C->d_work + (size_t)cfg.batch * cfg.q_heads * C->max_chunks * (D + 4);
   a.tickets = C->d_decode_tickets;
   a.err = C->d_err;
+  // the cache's fp16 rows (window, unsealed groups) are read straight from
+  // global memory, prefetched into L2 when their tile is issued
+  a.stage_f16 = 0;
   const DecLayout L = dec_layout(D, rep, C->k.bits, C->k.axis, C->k.whole, C->k.gpt, C->k.meta_bytes, C->v.bits,
-                                 C->v.axis, C->v.whole, C->v.gpt, C->v.meta_bytes);
+                                 C->v.axis, C->v.whole, C->v.gpt, C->v.meta_bytes, 0);
   a.st_kc = L.st_kc;
   a.st_km = L.st_km;
   a.st_vc = L.st_vc;
@@ -221,7 +224,7 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   return e;
 }
 
-// Decode over fp16 K / V rows materialised by kvq_dequantize ([B][Hkv][max_tokens][D]):
+// Decode over fp16 K / V rows materialised by kvq_dequantize ([B][Hkv][tcap][D]):
 // the same kernel (runtime formats, per-channel axis for both tensors) with
 // every token in its fp16 tail path, i.e. no packed tiles and no metadata.
 cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16, const void* v16, const void* q,
@@ -239,15 +242,16 @@ cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16,
     d.tail = static_cast<const __half*>(rows);
     d.axis = 1;
     d.whole = 0;
-    d.group = cfg.max_tokens;  // row stride of a (sequence, head)
+    d.group = C->tcap;         // row stride of a (sequence, head)
     d.lg_group = 30;           // nothing is ever sealed
     d.gpt = 0;
     d.window = 0;
-    d.ring = cfg.max_tokens;   // token t at row t
+    d.ring = C->tcap;          // token t at row t
   };
   tail_only(a.K, k16);
   tail_only(a.V, v16);
-  const DecLayout L = dec_layout(D, rep, a.K.bits, 1, 0, 0, a.K.meta_bytes, a.V.bits, 1, 0, 0, a.V.meta_bytes);
+  a.stage_f16 = 1;
+  const DecLayout L = dec_layout(D, rep, a.K.bits, 1, 0, 0, a.K.meta_bytes, a.V.bits, 1, 0, 0, a.V.meta_bytes, 1);
   a.st_kc = L.st_kc;
   a.st_km = L.st_km;
   a.st_vc = L.st_vc;

@@ -298,6 +298,7 @@ struct DynCfg {
   __device__ static int stage_off(const DecodeArgs& a) { return a.stage_off; }
   __device__ static int warp_bytes(const DecodeArgs& a) { return a.warp_bytes; }
   __device__ static int head_bytes(const DecodeArgs& a) { return a.head_bytes; }
+  __device__ static int stage_f16(const DecodeArgs& a) { return a.stage_f16; }
 };
 
 __host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
@@ -345,6 +346,7 @@ struct StatCfg {
   __device__ static constexpr int stage_off(const DecodeArgs&) { return L.stage_off; }
   __device__ static constexpr int warp_bytes(const DecodeArgs&) { return L.warp_bytes; }
   __device__ static constexpr int head_bytes(const DecodeArgs&) { return L.head_bytes; }
+  __device__ static constexpr int stage_f16(const DecodeArgs&) { return 0; }
 };
 
 // --------------------------------------------------------------- kernel ----
@@ -453,9 +455,22 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   auto lane_copy = [&](uint32_t sdst, const char* gsrc, int bytes) {
     for (int o = 0; o < bytes - lane * 16; o += 512) cp_async16_s(sdst + o, gsrc + o);
   };
+  const int f16st = CFG::stage_f16(a);
   auto issue = [&](int i) {
     const int t0 = w0 + i * kTile;
     const uint32_t sa = st_lane + (i & (ns - 1)) * stage_bytes;
+    // fp16 rows of the tile (16 consecutive ring rows): staged (materialised
+    // rows), else prefetched into L2 for the direct loads of the tile body
+    if (t0 >= sealed_k) {
+      const char* src = reinterpret_cast<const char*>(ktail + (long)(t0 % kring) * D);
+      if (f16st) lane_copy(sa + st_kc, src + lane * 16, 32 * D);
+      else for (int o = lane * 128; o < 32 * D; o += 32 * 128) prefetch_l2(src + o);
+    }
+    if (t0 >= sealed_v) {
+      const char* src = reinterpret_cast<const char*>(vtail + (long)(t0 % vring) * D);
+      if (f16st) lane_copy(sa + st_vc, src + lane * 16, 32 * D);
+      else for (int o = lane * 128; o < 32 * D; o += 32 * 128) prefetch_l2(src + o);
+    }
     if (t0 < sealed_k) {
       lane_copy(sa + st_kc, kc_g, kc_bytes);
       if (k_token || (t0 & kgmask) == 0) {  // per-token: every tile; per-channel: at a group's first tile
@@ -763,7 +778,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           // fp16 tail rows: token row R = g + 8*rh, channels 16j + 2tig + 8*kh (+1)
-          const __half* tb = ktail + (long)(t0 % kring) * D + 16 * j + 2 * tig;
+          const __half* tb = (f16st ? reinterpret_cast<const __half*>(st + st_kc) : ktail + (long)(t0 % kring) * D) +
+                             16 * j + 2 * tig;
           uint32_t A[4];
           A[0] = *reinterpret_cast<const uint32_t*>(tb + (long)g * D);
           A[1] = *reinterpret_cast<const uint32_t*>(tb + (long)(g + 8) * D);
@@ -951,7 +967,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           // fp16 rows: rows = channels 16j + g (+8), columns = tokens 2tig (+1) (+8)
-          const __half* tb = vtail + (long)(t0 % vring) * D + 16 * j + g;
+          const __half* tb = (f16st ? reinterpret_cast<const __half*>(st + st_vc) : vtail + (long)(t0 % vring) * D) +
+                             16 * j + g;
           auto pr = [&](int t, int coff) -> uint32_t {
             return pack_h2(tb[(long)t * D + coff], tb[(long)(t + 1) * D + coff]);
           };

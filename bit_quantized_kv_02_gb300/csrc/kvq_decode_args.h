@@ -49,6 +49,7 @@ struct DecodeArgs {
   int canon_k, canon_v;     // canonical (step, zero') entries per warp for per-token keys / values
   int stage_off;            // offset of the stage ring inside the per-warp region
   int head_bytes;           // CTA head region (q, group sums)
+  int stage_f16;            // fp16 rows (window, unsealed groups) are staged through the ring too
 };
 
 // Shared-memory plan of the decode kernel; one constexpr function serves the
@@ -63,17 +64,21 @@ struct DecLayout {
 __host__ __device__ constexpr int dl_round(int x, int m) { return (x + m - 1) / m * m; }
 __host__ __device__ constexpr int dl_max(int x, int y) { return x > y ? x : y; }
 
+// f16: stage slots also hold a 16-token tile of fp16 rows (32 * D bytes per tensor)
 __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, int kaxis, int kwhole, int kgpt,
-                                                   int kmb, int vbits, int vaxis, int vwhole, int vgpt, int vmb) {
+                                                   int kmb, int vbits, int vaxis, int vwhole, int vgpt, int vmb,
+                                                   int f16 = 0) {
   DecLayout L{};
   L.kc_bytes = D * kbits * 2;
   L.vc_bytes = D * vbits * 2;
+  const int kslot = f16 ? dl_max(L.kc_bytes, 32 * D) : L.kc_bytes;
+  const int vslot = f16 ? dl_max(L.vc_bytes, 32 * D) : L.vc_bytes;
   L.km_bytes = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) * kmb : D * kmb;
   L.vm_bytes = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) * vmb : D * vmb;
   L.st_kc = 0;
-  L.st_km = dl_round(L.st_kc + L.kc_bytes, 16);
+  L.st_km = dl_round(L.st_kc + kslot, 16);
   L.st_vc = dl_round(L.st_km + L.km_bytes, 16);
-  L.st_vm = dl_round(L.st_vc + L.vc_bytes, 16);
+  L.st_vm = dl_round(L.st_vc + vslot, 16);
   L.stage_bytes = dl_round(L.st_vm + L.vm_bytes, 128);
   L.lg_ns = L.stage_bytes <= 4096 ? 2 : 1;
   L.barea_bytes = (D / 16) * 32 * 8 * (rep == 8 ? 2 : 1);

@@ -740,9 +740,9 @@ cudaError_t launch_dequantize(kvq_cache* C, int layer, void* k_out, void* v_out,
     const dim3 grid((maxn + kTile * kWarps - 1) / (kTile * kWarps), H, B);
     __half* o = static_cast<__half*>(is_v ? v_out : k_out);
     const int D = C->cfg.head_dim;
-    if (D == 64) dequant_kernel<64><<<grid, 128, 0, st>>>(a, o, C->cfg.max_tokens);
-    else if (D == 128) dequant_kernel<128><<<grid, 128, 0, st>>>(a, o, C->cfg.max_tokens);
-    else dequant_kernel<256><<<grid, 128, 0, st>>>(a, o, C->cfg.max_tokens);
+    if (D == 64) dequant_kernel<64><<<grid, 128, 0, st>>>(a, o, C->tcap);
+    else if (D == 128) dequant_kernel<128><<<grid, 128, 0, st>>>(a, o, C->tcap);
+    else dequant_kernel<256><<<grid, 128, 0, st>>>(a, o, C->tcap);
     ++*launches;
   }
   return cudaGetLastError();

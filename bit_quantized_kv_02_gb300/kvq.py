@@ -219,10 +219,10 @@ class KVQCache:
 
     def kvq_dequantize(self, layer: int, k_out: torch.Tensor | None = None, v_out: torch.Tensor | None = None,
                        stream=None):
-        """Materialised baseline: fp16 K and V rows [batch][kv_heads][max_tokens][head_dim]
+        """Materialised baseline: fp16 K and V rows [batch][kv_heads][tcap][head_dim]
         of `layer` (rows past a sequence's length are left as they were)."""
         c = self.cfg
-        shape = (c.batch, c.kv_heads, c.max_tokens, c.head_dim)
+        shape = (c.batch, c.kv_heads, self.tcap, c.head_dim)
         if k_out is None:
             k_out = torch.zeros(shape, dtype=torch.float16, device=self.buffer.device)
         if v_out is None:

@@ -205,7 +205,7 @@ int kvq_cache_tcap(kvq_cache_t cache);
 kvq_status kvq_get_lens(kvq_cache_t cache, int layer, int32_t* lens_host);
 
 /* Materialised baseline, step 1: dequantize layer `layer` into fp16 rows
- * k_out, v_out [batch][kv_heads][max_tokens][head_dim] (device, 16-byte aligned; caller-owned;
+ * k_out, v_out [batch][kv_heads][tcap][head_dim] (tcap = kvq_cache_tcap(); device, 16-byte aligned; caller-owned;
  * token t of sequence b at row t; rows >= the sequence's length are not
  * written): x_hat = z + code * s as one fp32 fma (asymmetric), (code -
  * 2^(B-1)) * s (symmetric), the stored fp16 value for tail tokens, rounded to
@@ -219,7 +219,7 @@ kvq_status kvq_dequantize(kvq_cache_t cache, int layer, void* k_out, void* v_out
 
 /* Materialised baseline, step 2: decode attention (same definition, query
  * layout, scale and output as kvq_decode_attn) over fp16 rows k16, v16 in the
- * kvq_dequantize layout, for the lengths of `layer` in `cache`.  Uses the same
+ * kvq_dequantize layout (16-byte aligned), for the lengths of `layer` in `cache`.  Uses the same
  * split-K kernel with every token read as fp16 (no packed codes, no metadata)
  * and the cache's workspace, so it must not overlap a kvq_decode_attn on the
  * same cache. */
