@@ -80,18 +80,19 @@ def test_capacity_and_buffer_checks(L):
     assert L.kvq_append(None, 0, None, None, 0, None) == 1
 
 
+@pytest.mark.parametrize("window", [0, 64])
 @pytest.mark.parametrize("k,v,meta_f32", [
     ((4, 32, 1, 0), (4, 32, 0, 0), 0), ((2, 64, 1, 0), (2, 64, 0, 0), 0), ((6, 64, 0, 0), (4, 64, 0, 0), 0),
     ((3, -1, 0, 1), (8, 128, 1, 1), 1), ((5, 16, 1, 0), (7, -1, 0, 0), 0),
 ])
-def test_byte_accounting_matches_oracle(L, k, v, meta_f32):
+def test_byte_accounting_matches_oracle(L, k, v, meta_f32, window):
     H, D, B, layers = 3, 128, 4, 2
     cfg = _cfg(layers=layers, batch=B, kv_heads=H, q_heads=H * 2, head_dim=D, max_tokens=300, k=k, v=v,
-               meta_dtype=meta_f32)
+               meta_dtype=meta_f32, recent_window=window)
     lens = [0, 17, 200, 300]
     b = kvq.kvq_cache_bytes(cfg, lens)
-    pk, mk, tk = oracle.tensor_bytes(B, H, D, np.array(lens), k[0], k[1], k[2], bool(k[3]), bool(meta_f32))
-    pv, mv, tv = oracle.tensor_bytes(B, H, D, np.array(lens), v[0], v[1], v[2], bool(v[3]), bool(meta_f32))
+    pk, mk, tk = oracle.tensor_bytes(B, H, D, np.array(lens), k[0], k[1], k[2], bool(k[3]), bool(meta_f32), window)
+    pv, mv, tv = oracle.tensor_bytes(B, H, D, np.array(lens), v[0], v[1], v[2], bool(v[3]), bool(meta_f32), window)
     assert b.packed == layers * (pk + pv)
     assert b.metadata == layers * (mk + mv)
     assert b.tail == layers * (tk + tv)
