@@ -387,35 +387,20 @@ __device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, 
     }
     __syncwarp();
   }
-  for (int hh = 0; hh < nh; ++hh) {
+  // each lane ORs the bits of its channels' codes into the words that hold
+  // them (the token row's bits are zero: the tile was cleared at its first
+  // token), fire-and-forget with no read of the old words
+  for (int i = lane; i < rowlen; i += 32) {
+    const int hh = i / D, c = i - hh * D;
+    const uint32_t code = cs[i];
+    const FragPos f = elem_pos(a.is_value, trow, c);
     uint32_t* dst = codes_ptr(a, b, h + hh, tile);
-    const uint8_t* tc = cs + hh * D;
     for (int p = 0; p < pl.n; ++p) {
-      const int w = pl.w[p], off = pl.off[p];
-      const int W = D * w / 64, P = 16 / w;
-      const uint32_t mk = (1u << w) - 1u;
-      // keys: the 4 lanes of fragment row trow; values: the 8 lanes of fragment column trow
-      const int nl = a.is_value ? 8 : 4;
-      for (int idx = lane; idx < nl * W; idx += 32) {
-        const int li = idx / W, i = idx % W;
-        const int ln = a.is_value ? (4 * li + ((trow & 7) >> 1)) : (4 * (trow & 7) + li);
-        uint32_t m = 0, nv = 0;
-        for (int k = 0; k < P; ++k)
-          for (int e = 0; e < 2; ++e) {
-            int t, c;
-            elem_of(a.is_value, ln, i * P + k, e, &t, &c);
-            if (t == trow) {
-              m |= mk << (k * w + 16 * e);
-              nv |= (((uint32_t)tc[c] >> off) & mk) << (k * w + 16 * e);
-            }
-          }
-        if (!m) continue;
-        const int wi = D * off / 2 + ln * W + i;
-        // the row's bits are zero (the tile was cleared at its first token), so
-        // the merge is a fire-and-forget OR with no read of the old word
-        if (trow == 0) dst[wi] = nv;
-        else atomicOr(dst + wi, nv);
-      }
+      const int w = pl.w[p], lw = w == 1 ? 0 : (w == 2 ? 1 : (w == 4 ? 2 : 3));
+      const int word = D * pl.off[p] / 2 + f.lane * (D >> (6 - lw)) + (f.pi >> (4 - lw));
+      const int bit = ((f.pi & ((16 >> lw) - 1)) << lw) + 16 * f.e;
+      const uint32_t v = ((code >> pl.off[p]) & ((1u << w) - 1u)) << bit;
+      if (v) atomicOr(dst + word, v);
     }
   }
   if (lane == 0 && smax_local > 0.0f)
