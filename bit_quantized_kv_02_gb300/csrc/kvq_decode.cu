@@ -15,6 +15,32 @@ struct Plan {
   dim3 grid;
 };
 
+// Shared memory a cluster launch adds after the kernel's plan: the first
+// CTA's gather area of the csize split partials ([csize][rep][D+2] floats).
+static size_t gather_bytes(int csize, int rep, int D) { return (size_t)csize * rep * (D + 2) * 4; }
+
+// Raise (never lower) a kernel's dynamic shared-memory limit: several caches
+// may share one kernel with different plans.
+static cudaError_t raise_smem_limit(const void* fn, size_t bytes) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, fn);
+  if (e != cudaSuccess) return e;
+  if ((size_t)fa.maxDynamicSharedSizeBytes >= bytes) return cudaSuccess;
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// Whether a cluster launch of fn keeps the residency the planner counts on
+// (min(occ, 4) CTAs per SM) with the largest gather area added.
+static bool cluster_fits(const void* fn, size_t smem, int rep, int D, int occ, int warp_bytes) {
+  const size_t full = smem + gather_bytes(kMaxCluster, rep, D);
+  if (full > 227 * 1024) return false;
+  if (4L * rep * (D + 2) * 4 > 4L * warp_bytes) return false;  // the CTA merge's four warp partials
+  if (raise_smem_limit(fn, full) != cudaSuccess) return false;
+  int occ2 = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ2, fn, kWarps * 32, full) != cudaSuccess) return false;
+  return occ2 >= std::min(occ, 4);
+}
+
 void* pick_kernel(int D, bool r8, int vaxis) {
   if (D == 64) return decode_kernel_ptr_d64(r8, vaxis);
   if (D == 128) return decode_kernel_ptr_d128(r8, vaxis);
@@ -104,7 +130,7 @@ cudaError_t decode_setup(kvq_cache* C) {
   cudaError_t e = make_plan(C, 0, &P, &occ);
   if (e != cudaSuccess) return e;
   if (P.smem > 227 * 1024) return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.smem);
+  e = raise_smem_limit(fn, P.smem);
   if (e != cudaSuccess) return e;
   // the same (largest) shared-memory carve-out as the append kernel, so that
   // alternating append / decode launches need no L1 / shared reconfiguration
@@ -114,11 +140,8 @@ cudaError_t decode_setup(kvq_cache* C) {
   if (e != cudaSuccess) return e;
   C->dec_smem = P.smem;
   C->dec_occ = std::max(occ, 1);
-  // the cluster combine keeps the CTA partial and its staging after the four
-  // warp partials in the merge area (the per-warp regions)
-  const int rep = C->cfg.q_heads / C->cfg.kv_heads, rowlen = C->cfg.head_dim + 2;
-  const long need = (5L * rep * rowlen + 2L * rep * kMaxCluster + rep) * 4;
-  C->dec_cluster_ok = need <= 4L * P.a.warp_bytes && !C->global_combine;
+  const int rep = C->cfg.q_heads / C->cfg.kv_heads;
+  C->dec_cluster_ok = !C->global_combine && cluster_fits(fn, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
   return cudaSuccess;
 }
 
@@ -191,6 +214,8 @@ static cudaError_t plan_launch(kvq_cache* C, int layer, const void* q, int q_f32
   // that wait for their cluster would hold slots that later CTAs need)
   const long ctas = (long)nch * cfg.kv_heads * cfg.batch;
   a.csize = (C->dec_cluster_ok && nch <= kMaxCluster && ctas <= slots) ? nch : 0;
+  a.gath_off = (int)P->smem;
+  P->smem += gather_bytes(a.csize, cfg.q_heads / cfg.kv_heads, cfg.head_dim);
   a.q = q;
   a.q_f32 = q_f32;
   a.scale_log2 = scale * 1.4426950408889634f;
@@ -206,7 +231,7 @@ cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, flo
   cudaError_t e = plan_launch(C, layer, q, q_f32, scale, out, &P, &grid);
   if (e != cudaSuccess) return e;
   void* args[] = {&P.a};
-  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), C->dec_smem, st, args, P.a.csize);
+  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), P.smem, st, args, P.a.csize);
   ++*launches;
   return e;
 }
@@ -225,7 +250,7 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   a.gwork = work + (size_t)C->cfg.batch * C->cfg.q_heads * C->max_chunks * (C->cfg.head_dim + 4);
   a.tickets = tickets;
   void* args[] = {&a};
-  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), C->dec_smem, st, args, a.csize);
+  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), P.smem, st, args, a.csize);
   ++*launches;
   return e;
 }
@@ -271,7 +296,8 @@ cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16,
   a.warp_bytes = L.warp_bytes;
   a.head_bytes = L.head_bytes;
   const size_t smem = (size_t)a.head_bytes + (size_t)kWarps * a.warp_bytes;
-  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  e = raise_smem_limit(fn, smem);
   if (e != cudaSuccess) return e;
   int occ = 1;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kWarps * 32, smem);
@@ -284,15 +310,18 @@ cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16,
   int maxn = 0;
   for (int b = 0; b < cfg.batch; ++b) maxn = std::max(maxn, (int)plan[b]);
   const int nch = std::max(1, (maxn + a.S - 1) / a.S);
-  const long need = (5L * rep * (D + 2) + 2L * rep * kMaxCluster + rep) * 4;
   const long ctas = (long)nch * cfg.kv_heads * cfg.batch;
-  a.csize = (!C->global_combine && need <= 4L * a.warp_bytes && nch <= kMaxCluster && ctas <= slots) ? nch : 0;
+  const bool cl_ok = !C->global_combine && nch <= kMaxCluster && ctas <= slots &&
+                     cluster_fits(fn, smem, rep, D, std::max(occ, 1), a.warp_bytes);
+  a.csize = cl_ok ? nch : 0;
+  a.gath_off = (int)smem;
+  const size_t lsmem = smem + gather_bytes(a.csize, rep, D);
   a.q = q;
   a.q_f32 = q_f32;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.out = out;
   void* args[] = {&a};
-  e = launch_pdl(fn, dim3(nch, cfg.kv_heads, cfg.batch), dim3(kWarps * 32), smem, st, args, a.csize);
+  e = launch_pdl(fn, dim3(nch, cfg.kv_heads, cfg.batch), dim3(kWarps * 32), lsmem, st, args, a.csize);
   ++*launches;
   return e;
 }

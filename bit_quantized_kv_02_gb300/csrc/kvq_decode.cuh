@@ -369,6 +369,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const int rep = CFG::rep(a), H = a.H, S = a.S;
+  // cluster launch: this arrival tells the cluster that this CTA runs; the
+  // matching wait comes before the first store into another CTA's shared memory
+  if (a.csize) cluster_arrive_relaxed();
   pdl_wait();  // the cache and the query are complete
   const int hq0 = h * rep;
   // the query and the largest steps are requested before the length, so the
@@ -1136,12 +1139,19 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     }
   }
   __syncthreads();
-  // CTA merge -> chunk partial in the workspace (cluster launch: in shared
-  // memory after the four warp partials)
-  float* part = mw + kWarps * rep * rowlen;
+  // CTA merge -> chunk partial in the workspace (cluster launch: straight
+  // into the gather area of the cluster's first CTA)
   constexpr int wrow = D + 4;  // workspace row: D outputs, m, l, two pad (16-byte aligned rows)
   const long hqb = (long)b * H * rep + hq0;
   const int max_chunks = a.max_chunks;
+  namespace cg = cooperative_groups;
+  float* gath = reinterpret_cast<float*>(smem + a.gath_off);  // [csize][rep][rowlen] (first CTA)
+  float* part = gath;
+  if (a.csize) {
+    cg::cluster_group cl = cg::this_cluster();
+    part = cl.map_shared_rank(gath, 0) + (int)cl.block_rank() * rep * rowlen;
+    cluster_wait();  // every CTA of the cluster has started: its shared memory may be written
+  }
   for (int i = threadIdx.x; i < rep * rowlen; i += blockDim.x) {
     const int rho = i / rowlen, c = i % rowlen;
     float M = -INFINITY;
@@ -1162,44 +1172,28 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   }
   if (a.csize) {
     // Cluster merge: the splits of this (sequence, head) are the CTAs of one
-    // cluster; each CTA reads every CTA's partial through distributed shared
-    // memory and writes its share of the output columns.
-    namespace cg = cooperative_groups;
+    // cluster and have stored their partials (m_k, l_k, O_k) in the first
+    // CTA's gather area; once the barrier has made them visible, that CTA
+    // merges them and the others leave (nobody reads their shared memory).
     cg::cluster_group cl = cg::this_cluster();
+    cl.sync();
+    if (cl.block_rank() != 0) return;
     const int K = a.csize;
-    const int crank = (int)cl.block_rank();
-    float* cw = part + rep * rowlen;  // [rep][K] m_k, then weights
-    float* cl_l = cw + rep * K;       // [rep][K] l_k
-    float* cden = cl_l + rep * K;     // [rep]
-    cl.sync();  // every partial of the cluster is complete and visible
-    for (int i = threadIdx.x; i < rep * K; i += blockDim.x) {
-      const int rho = i / K, k = i - rho * K;
-      const float* rp = cl.map_shared_rank(part, k);
-      cw[i] = rp[rho * rowlen + D];
-      cl_l[i] = rp[rho * rowlen + D + 1];
-    }
-    __syncthreads();
-    for (int rho = threadIdx.x; rho < rep; rho += blockDim.x) {
-      float M = -INFINITY;
-      for (int k = 0; k < K; ++k) M = fmaxf(M, cw[rho * K + k]);
-      float den = 0.0f;
-      for (int k = 0; k < K; ++k) {
-        const float mk = cw[rho * K + k];
-        const float f = (mk == -INFINITY) ? 0.0f : fast_exp2(mk - M);
-        den += f * cl_l[rho * K + k];
-        cw[rho * K + k] = f;
-      }
-      cden[rho] = den;
-    }
-    __syncthreads();
-    for (int i = crank * blockDim.x + threadIdx.x; i < rep * D; i += K * blockDim.x) {
+    for (int i = threadIdx.x; i < rep * D; i += blockDim.x) {
       const int rho = i / D, c = i - rho * D;
-      float num = 0.0f;
-      for (int k = 0; k < K; ++k) num += cw[rho * K + k] * cl.map_shared_rank(part, k)[rho * rowlen + c];
-      const float den = cden[rho];
+      const float* pr = gath + rho * rowlen;
+      float M = -INFINITY;
+      for (int k = 0; k < K; ++k) M = fmaxf(M, pr[k * rep * rowlen + D]);
+      float num = 0.0f, den = 0.0f;
+      for (int k = 0; k < K; ++k) {
+        const float* pk = pr + k * rep * rowlen;
+        const float mk = pk[D];
+        const float f = (mk == -INFINITY) ? 0.0f : fast_exp2(mk - M);
+        den += f * pk[D + 1];
+        num += f * pk[c];
+      }
       a.out[(hqb + rho) * D + c] = den > 0.0f ? num / den : 0.0f;
     }
-    cl.sync();  // no CTA leaves while others may still read its partial
     return;
   }
   // Two-level combine behind atomic tickets (no CTA ever waits): the last CTA

@@ -38,6 +38,8 @@ struct DecodeArgs {
   int max_groups;           // ceil(max_chunks / kCombineGroup)
   int csize;                // > 0: the grid's x dimension forms clusters of csize CTAs (all splits of one
                             // sequence and head) that merge through distributed shared memory
+  int gath_off;             // cluster launch: byte offset of [csize][rep][D+2] split partials, gathered in
+                            // the cluster's first CTA (after the per-warp regions)
   uint32_t* tickets;        // [B][H][1 + max_groups]: head ticket, then one per chunk group
   float* out;               // [B][H*rep][D]
   int* err;
