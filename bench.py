@@ -1,8 +1,10 @@
 """Benchmark: quantized KV-cache decode step on GB300.
 
-One step = for every layer of the workload: kvq_append (one new token per
-sequence: quantize / stage / seal) then kvq_decode_attn (split-K attention over
-the packed cache).  The default workload is the GPT-2-small-shaped cache (12
+One step = for every layer of the workload: kvq_append_decode_attn, i.e. the
+append of one new token per sequence (quantize / stage / seal) and the split-K
+attention over the packed cache, in one launch (the format's fused decode
+specialisation; formats without one run kvq_append then kvq_decode_attn).
+The default workload is the GPT-2-small-shaped cache (12
 layers, batch 8, 12 heads, head_dim 64, 2048 cached tokens, fp16 N(0,1) with
 1% of key channels x10), K 4-bit per-channel G=32 / V 4-bit per-token G=32.
 
@@ -256,21 +258,22 @@ def run_ours(args, rank, world):
     kin.copy_(kin_all[0])
     qin.copy_(q_all[0])
     torch.cuda.synchronize()
-    # the step: per layer kvq_append then kvq_decode_attn; consecutive launches
-    # overlap their launch latency (programmatic dependent launch), so the graph
-    # holds no timing events between them
+    # the step: per layer the append fused into the decode launch; consecutive
+    # launches overlap their launch latency (programmatic dependent launch), so
+    # the graph holds no timing events between them
     graph = torch.cuda.CUDAGraph()
+    launches_per_step = 0
     with torch.cuda.graph(graph, stream=stream):
         for l in range(L):
-            cache.kvq_append(l, kin[l, 0], kin[l, 1], stream=stream)
-            cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
+            cache.kvq_append_decode_attn(l, kin[l, 0], kin[l, 1], qin[l], out[l], scale, stream=stream)
+            launches_per_step += cache.kvq_last_launches()
+    cache.kvq_refresh_lens(stream)  # capturing launched nothing
     # the decode kernel alone: the step's L decode launches back to back (same
     # inputs, same cache state), timed as a whole after its own L2 flush
     graph_dec = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph_dec, stream=stream):
         for l in range(L):
             cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
-    launches_per_step = 2 * L
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = None
@@ -391,7 +394,7 @@ def run_ours(args, rank, world):
                        "batch_per_gpu": B, "q_heads": Hq, "kv_heads": H, "recent_window": args.window,
                        "head_dim": D, "cached_tokens": wl.lens[0], "k": list(wl.k), "v": list(wl.v),
                        "k_format": "bits,group,axis(0 per-token,1 per-channel),mode(0 asym,1 sym)",
-                       "step": "per layer: kvq_append + kvq_decode_attn (CUDA graph)",
+                       "step": "per layer: kvq_append_decode_attn (append fused into the decode launch; CUDA graph)",
                        "l2": "256 MB buffer written before every timed step (L2 flushed)",
                        "parallelism": f"dp{world} (sequences sharded, no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -406,7 +409,7 @@ def run_ours(args, rank, world):
             "gpu_launches": launches_per_step * steps,
             "e2e": {"value": round(bytes_e2e_all / (t_e2e_max * 1e-3) / 1e9, 2) if e2e_steps else None,
                     "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "path": "pinned host -> device copies, graph of kvq_append + kvq_decode_attn, device -> host"},
+                    "path": "pinned host -> device copies, graph of kvq_append_decode_attn, device -> host"},
             "clocks": clk,
         }
         if mat is not None:

@@ -127,6 +127,8 @@ size_t carve(const kvq_config& c, kvq_cache* C) {
   off += align256((size_t)2 * L * B * H * 4);
   size_t hl_off = off;
   off += align256((size_t)L * B * H * 4);
+  size_t ar_off = off;
+  off += align256((size_t)B * H * 4);
   const int mc = max_chunks_of(c, tcap);
   size_t dt_off = off;
   off += align256(decode_ticket_words(B, H, mc) * 4);
@@ -142,6 +144,7 @@ size_t carve(const kvq_config& c, kvq_cache* C) {
     C->d_lens = reinterpret_cast<int32_t*>(C->base + lens_off);
     C->d_smax = reinterpret_cast<uint32_t*>(C->base + smax_off);
     C->d_head_lens = reinterpret_cast<int32_t*>(C->base + hl_off);
+    C->d_arrive = reinterpret_cast<uint32_t*>(C->base + ar_off);
     C->d_decode_tickets = reinterpret_cast<uint32_t*>(C->base + dt_off);
     C->d_err = reinterpret_cast<int*>(C->base + err_off);
     C->d_work = reinterpret_cast<float*>(C->base + work_off);
@@ -294,6 +297,39 @@ kvq_status kvq_decode_attn(kvq_cache_t C, int layer, const void* q, int q_dtype,
   cudaError_t e = launch_decode(C, layer, q, q_dtype == KVQ_F32, softmax_scale, out,
                                 static_cast<cudaStream_t>(stream), &C->last_launches);
   return cuda_status(C, e);
+}
+
+kvq_status kvq_append_decode_attn(kvq_cache_t C, int layer, const void* k_new, const void* v_new, int in_dtype,
+                                  const void* q, int q_dtype, float softmax_scale, float* out, void* stream) {
+  kvq_status s = layer_ok(C, layer);
+  if (s != KVQ_OK) return s;
+  if (!k_new || !v_new || (in_dtype != KVQ_F16 && in_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
+  if (!q || !out || (q_dtype != KVQ_F16 && q_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.0f)) softmax_scale = 1.0f / std::sqrt((float)C->cfg.head_dim);
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  int32_t* lens = C->lens.data() + (long)layer * C->cfg.batch;
+  for (int b = 0; b < C->cfg.batch; ++b)
+    if (lens[b] + 1 > C->cfg.max_tokens) return KVQ_ERR_CAPACITY;
+  C->last_launches = 0;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the fused append reads each lane's channels as 4- / 8-byte pairs
+  const bool aligned = (reinterpret_cast<uintptr_t>(k_new) % 8) == 0 && (reinterpret_cast<uintptr_t>(v_new) % 8) == 0;
+  if (!C->fused_ok || !aligned) {
+    cudaError_t e = launch_append(C, layer, k_new, v_new, in_dtype == KVQ_F32, st, &C->last_launches);
+    if (e != cudaSuccess) return cuda_status(C, e);
+    for (int b = 0; b < C->cfg.batch; ++b) lens[b] += 1;
+    e = launch_decode(C, layer, q, q_dtype == KVQ_F32, softmax_scale, out, st, &C->last_launches);
+    return cuda_status(C, e);
+  }
+  // the launch is planned for the new lengths
+  for (int b = 0; b < C->cfg.batch; ++b) lens[b] += 1;
+  cudaError_t e = launch_append_decode(C, layer, k_new, v_new, in_dtype == KVQ_F32, q, q_dtype == KVQ_F32,
+                                       softmax_scale, out, st, &C->last_launches);
+  if (e != cudaSuccess) {
+    for (int b = 0; b < C->cfg.batch; ++b) lens[b] -= 1;
+    return cuda_status(C, e);
+  }
+  return KVQ_OK;
 }
 
 kvq_status kvq_dequantize(kvq_cache_t C, int layer, void* k_out, void* v_out, void* stream) {

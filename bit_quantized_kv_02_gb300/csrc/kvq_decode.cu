@@ -100,6 +100,7 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   // the cache's fp16 rows (window, unsealed groups) are read straight from
   // global memory, prefetched into L2 when their tile is issued
   a.stage_f16 = 0;
+  a.arrive = C->d_arrive;
   const DecLayout L = dec_layout(D, rep, C->k.bits, C->k.axis, C->k.whole, C->k.gpt, C->k.meta_bytes, C->v.bits,
                                  C->v.axis, C->v.whole, C->v.gpt, C->v.meta_bytes, 0);
   a.st_kc = L.st_kc;
@@ -142,6 +143,25 @@ cudaError_t decode_setup(kvq_cache* C) {
   C->dec_occ = std::max(occ, 1);
   const int rep = C->cfg.q_heads / C->cfg.kv_heads;
   C->dec_cluster_ok = !C->global_combine && cluster_fits(fn, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
+  // the fused append needs a fused specialisation, layouts where each
+  // (sequence, head) owns all it writes (no window, no whole-vector groups),
+  // its scratch inside one warp's stage ring, and the plain kernel's
+  // residency and cluster merge (the launch is planned for the plain kernel)
+  const int ring = (1 << P.a.lg_nstages) * P.a.stage_bytes;
+  C->fused_ok = 0;
+  C->dec_fn_fused = C->generic_decode ? nullptr : decode_kernel_fused(C);
+  if (C->dec_fn_fused && C->k.window == 0 && C->v.window == 0 && !C->k.whole && !C->v.whole &&
+      fused_append_scratch(C->cfg.head_dim, C->k.axis, C->v.axis) <= ring) {
+    void* ff = C->dec_fn_fused;
+    int occ_f = 0;
+    e = raise_smem_limit(ff, P.smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(ff, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_f, ff, kWarps * 32, P.smem);
+    if (e != cudaSuccess) return e;
+    const bool cl_same =
+        !C->dec_cluster_ok || cluster_fits(ff, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
+    C->fused_ok = occ_f >= C->dec_occ && cl_same;
+  }
   return cudaSuccess;
 }
 
@@ -232,6 +252,21 @@ cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, flo
   if (e != cudaSuccess) return e;
   void* args[] = {&P.a};
   e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), P.smem, st, args, P.a.csize);
+  ++*launches;
+  return e;
+}
+
+// Append of one token per (sequence, head) fused into the decode launch.  The
+// host mirror of the lengths already counts the new token.
+cudaError_t launch_append_decode(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, const void* q,
+                                 int q_f32, float scale, float* out, cudaStream_t st, int* launches) {
+  Plan P;
+  dim3 grid;
+  cudaError_t e = plan_launch(C, layer, q, q_f32, scale, out, &P, &grid);
+  if (e != cudaSuccess) return e;
+  P.a.ap = make_append_args(C, layer, k, v, x_f32);
+  void* args[] = {&P.a};
+  e = launch_pdl(C->dec_fn_fused, grid, dim3(kWarps * 32), P.smem, st, args, P.a.csize);
   ++*launches;
   return e;
 }

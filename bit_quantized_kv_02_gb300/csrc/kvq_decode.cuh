@@ -38,6 +38,7 @@
 #include <cooperative_groups.h>
 
 #include "kvq_decode_args.h"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 
@@ -357,7 +358,9 @@ __host__ __device__ constexpr int decode_min_blocks(int D, bool is_static) {
   return is_static ? (D == 64 ? 5 : (D == 128 ? 4 : 2)) : (D == 64 ? 5 : (D == 128 ? 3 : 2));
 }
 
-template <int D, bool R8, int VAXIS, class CFG>
+// FUSED: the launch also appends the new token (kvq_append_decode_attn); the
+// plain decode kernel is compiled without any of that code.
+template <int D, bool R8, int VAXIS, class CFG, bool FUSED = false>
 __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages != 0)) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NCH = D / 16;                // 16-channel chunks / m-tiles
@@ -386,10 +389,32 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     if (i < rep * D)
       qv[u] = a.q_f32 ? reinterpret_cast<const float*>(a.q)[qi] : __half2float(reinterpret_cast<const __half*>(a.q)[qi]);
   }
-  const float smax_k = __uint_as_float(a.smax_k[(long)b * H + h]);
-  const float smax_v = __uint_as_float(a.smax_v[(long)b * H + h]);
-  const int n = a.lens[b];
+  float smax_k = __uint_as_float(a.smax_k[(long)b * H + h]);
+  float smax_v = __uint_as_float(a.smax_v[(long)b * H + h]);
+  // fused append: the cache holds n_old tokens of this (sequence, head) and
+  // this launch appends token n_old, then attends over n_old + 1 tokens; the
+  // new rows head for L2 now, so the appending warp finds them there
+  if (FUSED && warp == 0) {
+    const int row_bytes = D * (a.ap.k.x_f32 ? 4 : 2);
+    const long xo = ((long)b * H + h) * row_bytes;
+    if (lane * 128 < row_bytes) prefetch_l2(static_cast<const char*>(a.ap.k.x) + xo + lane * 128);
+    if (lane * 128 < row_bytes) prefetch_l2(static_cast<const char*>(a.ap.v.x) + xo + lane * 128);
+  }
+  const int n_old = FUSED ? a.ap.head_lens[(long)b * H + h] : 0;
+  const int n = FUSED ? n_old + 1 : a.lens[b];
   const int nchunks = (n + S - 1) / S;
+  // every CTA of (b, h) counts itself in once it has its old length (the
+  // length is consumed first: the count cannot pass the read); the last one
+  // advances the lengths, which no CTA of this launch reads afterwards
+  unsigned arrival = 0u;
+  if (FUSED && threadIdx.x == 0 && nchunks > 0) arrival = atomicAdd(a.arrive + (long)b * H + h, 1u);
+  auto advance_lengths = [&]() {
+    if (FUSED && threadIdx.x == 0 && arrival == gridDim.x - 1u) {
+      a.ap.head_lens[(long)b * H + h] = n;
+      if (h == 0) a.ap.lens[b] = n;
+      a.arrive[(long)b * H + h] = 0u;
+    }
+  };
   // (in a cluster launch every CTA takes part in the merge: splits past the
   // sequence's end just contribute empty partials)
   if (!a.csize) {
@@ -398,7 +423,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         for (int i = threadIdx.x; i < rep * D; i += blockDim.x) a.out[((long)b * H * rep + hq0) * D + i] = 0.0f;
       return;
     }
-    if (chunk >= nchunks) return;
+    if (chunk >= nchunks) {
+      advance_lengths();
+      return;
+    }
   }
 
   // ---- tensor formats (constants in a compile-time configuration)
@@ -425,6 +453,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   unsigned char* stages = wbase + CFG::stage_off(a);
 
   // ---- this warp's token range and its copy sources
+  // (fused append: the warp whose range holds token n_old appends it before
+  // it stages anything; its range holds every tile and group the append
+  // writes, so no other warp or CTA reads them)
+  const bool appender = FUSED && chunk == n_old / S && warp == (n_old - chunk * S) / a.Sw;
   const int w0 = chunk * S + warp * a.Sw;
   const int w1 = min(w0 + a.Sw, n);
   const int ntl = w1 > w0 ? (w1 - w0 + kTile - 1) / kTile : 0;
@@ -496,10 +528,30 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   // overlaps it
   // (one commit group per stage, empty past the range's end, so that the
   // group of tile i is always the (i+1)-th oldest)
-  for (int i = 0; i < ns; ++i) {
-    if (i < ntl) issue(i);
-    cp_async_commit();
+  auto issue_first = [&](int i0, int i1) {
+    for (int i = i0; i < i1; ++i) {
+      if (i < ntl) issue(i);
+      cp_async_commit();
+    }
+  };
+  // the appending warp stages at once the tiles below the first one the
+  // append writes (a per-token tensor: the new token's tile; a per-channel
+  // tensor: the group it seals, if it seals one) and the rest after it; the
+  // append's scratch is the ring's slots from `early` on, which hold nothing
+  // until then
+  int early = ns;
+  if (appender) {
+    const bool seal_k = !k_token && ((n_old + 1) & (kG - 1)) == 0;
+    const bool seal_v = VAXIS == 1 && ((n_old + 1) & (vG - 1)) == 0;
+    int prot = 0x7fffffff;
+    if (k_token) prot = min(prot, n_old & ~(kTile - 1));
+    else if (seal_k) prot = min(prot, n_old + 1 - kG);
+    if (VAXIS == 0) prot = min(prot, n_old & ~(kTile - 1));
+    else if (seal_v) prot = min(prot, n_old + 1 - vG);
+    const int need = (seal_k || seal_v) ? 40 * D : 0;
+    early = min(min(ns, max(0, (prot - w0) / kTile)), ns - (need + stage_bytes - 1) / stage_bytes);
   }
+  issue_first(0, early);
 
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {
@@ -519,6 +571,18 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   for (int i = lane; i < CFG::barea_bytes(a) / 4; i += 32) barea[i] = 0u;
   if (lane < 8) wbias[lane] = 0.0f;
   __syncthreads();
+  if (FUSED && appender) {
+    // append into the cache (scratch: this warp's idle stage ring), make the
+    // writes visible to the copies that follow, then stage the first tiles;
+    // this warp's step bounds include the steps just written
+    float kst, vst;
+    fused_append<D>(a.ap, b, h, n_old, stages + early * stage_bytes, &kst, &vst);
+    smax_k = fmaxf(smax_k, kst);
+    smax_v = fmaxf(smax_v, vst);
+    __threadfence_block();  // only this warp reads what it wrote
+    __syncwarp();
+    issue_first(early, ns);
+  }
 
 
   // ---- per-warp state
@@ -1042,6 +1106,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   cp_async_wait<0>();  // (only empty groups remain) before the stages are reused
 
   pdl_trigger();  // only the merge and the combine remain: the next kernel may start launching
+  advance_lengths();
 
   // ---- warp epilogue: complete l and the per-token value zero-point sums
 #pragma unroll

@@ -22,6 +22,27 @@ struct DecTensor {
   int ring;             // fp16 rows per (sequence, head): token t at row t % ring
 };
 
+// Arguments of the quantizer kernels for one layer-tensor.
+struct QuantArgs {
+  TensorLayout L;
+  int is_value;
+  int layer, B, H, D, tcap, ntiles;
+  const void* x;  // [B][t_stride][H][D]
+  int x_f32;
+  long t_stride;
+  const int32_t* lens;  // device lens of this layer
+  char* base;           // cache buffer
+  uint32_t* smax;       // [B][H] for this tensor and layer
+};
+
+// Append of one token per (sequence, kv head) to both tensors of a layer.
+struct AppendArgs {
+  QuantArgs k, v;       // x points at [B][H][D] new tokens (t_stride unused)
+  int32_t* lens;        // device lens of the layer
+  int32_t* head_lens;   // [B][H] per-head length counters of the layer
+  int warp_smem;        // per-warp scratch bytes for the per-token path
+};
+
 struct DecodeArgs {
   DecTensor K, V;
   int B, H, rep, tcap, ntiles;
@@ -52,7 +73,23 @@ struct DecodeArgs {
   int stage_off;            // offset of the stage ring inside the per-warp region
   int head_bytes;           // CTA head region (q, group sums)
   int stage_f16;            // fp16 rows (window, unsealed groups) are staged through the ring too
+  // fused append (the kernel's FUSED instantiation, kvq_append_decode_attn):
+  // the warp whose range holds the new token appends it first; lengths come
+  // from ap.head_lens (old length + 1) and the last CTA of each (sequence,
+  // head) to count itself in `arrive` advances them
+  uint32_t* arrive;         // [B][H] arrival counters (zero between launches)
+  AppendArgs ap;
 };
+
+// Scratch bytes one warp needs for the fused append: a per-channel seal's
+// (2*D floats of group parameters + 16 rows of D halves); per-token tensors
+// need none.
+__host__ __device__ constexpr int fused_append_scratch(int D, int k_axis, int v_axis) {
+  return (k_axis == 1 || v_axis == 1) ? 40 * D : 0;
+}
+
+// Host: the append arguments of a layer (kvq_quant.cu).
+AppendArgs make_append_args(const kvq_cache* C, int layer, const void* k, const void* v, int x_f32);
 
 // Shared-memory plan of the decode kernel; one constexpr function serves the
 // host planner and the compile-time specialisations, so both always agree.

@@ -1,45 +1,9 @@
-// kvq_decode_fast.cu — compile-time specialisations of the decode kernel for
-// the cache formats of the benchmarked workloads (fp16 metadata, no
-// whole-vector groups).  Any other format runs the generic kernel.
-#include "kvq_decode.cuh"
+// kvq_decode_fast.cu — the plain compile-time specialisations of the decode
+// kernel.  Any other format runs the generic kernel.
+#include "kvq_decode_table.cuh"
 
 namespace kvq {
 
-namespace {
-
-struct FastEntry {
-  int D, rep, kb, kax, kg, ksym, vb, vax, vg, vsym;
-  void* fn;
-};
-
-template <int D, int REP, int KB, int KAX, int KG, int KSYM, int VB, int VAX, int VG, int VSYM>
-FastEntry entry() {
-  using C = StatCfg<D, REP, KB, KAX, KG, KSYM, VB, VAX, VG, VSYM>;
-  return {D, REP, KB, KAX, KG, KSYM, VB, VAX, VG, VSYM, reinterpret_cast<void*>(&decode_kernel<D, REP == 8, VAX, C>)};
-}
-
-}  // namespace
-
-void* decode_kernel_fast(const kvq_cache* C) {
-  // D, rep, K bits/axis/group/sym, V bits/axis/group/sym (axis 0 per token, 1 per channel)
-  static const FastEntry table[] = {
-      entry<64, 1, 4, 1, 32, 0, 4, 0, 32, 0>(),    // 4-bit, keys per channel / values per token, G=32
-      entry<64, 1, 6, 0, 64, 0, 4, 0, 64, 0>(),    // K6/V4 per-head 64-channel groups
-      entry<128, 1, 2, 1, 32, 0, 2, 0, 32, 0>(),   // 2-bit MHA, head_dim 128, G=32
-      entry<128, 4, 2, 1, 64, 0, 2, 0, 64, 0>(),   // 2-bit GQA 4:1, G=64
-      entry<256, 8, 4, 0, 32, 0, 8, 0, 32, 0>(),   // K4/V8 GQA 8:1, 32-channel groups
-      entry<256, 8, 4, 1, 32, 0, 8, 0, 32, 0>(),   // same with keys per channel
-      entry<256, 8, 6, 0, 32, 1, 6, 0, 32, 1>(),   // symmetric 6-bit
-  };
-  const kvq_config& c = C->cfg;
-  if (c.meta_dtype != KVQ_F16 || C->k.whole || C->v.whole) return nullptr;
-  const int rep = c.q_heads / c.kv_heads;
-  for (const FastEntry& e : table) {
-    if (e.D == c.head_dim && e.rep == rep && e.kb == c.k.bits && e.kax == c.k.axis && e.kg == c.k.group &&
-        e.ksym == c.k.mode && e.vb == c.v.bits && e.vax == c.v.axis && e.vg == c.v.group && e.vsym == c.v.mode)
-      return e.fn;
-  }
-  return nullptr;
-}
+void* decode_kernel_fast(const kvq_cache* C) { return lookup_specialised<false>(C); }
 
 }  // namespace kvq

@@ -32,6 +32,9 @@ struct kvq_cache {
   int global_combine = 0;  // 1: always merge split-K partials through the global workspace
   void* dec_fn = nullptr;  // decode kernel in use (compile-time specialisation or generic)
   int generic_decode = 0;  // 1: always use the generic (runtime-format) decode kernel
+  int fused_ok = 0;        // the append can run inside the decode launch (kvq_append_decode_attn)
+  void* dec_fn_fused = nullptr;  // the decode kernel's specialisation with the append fused in
+  uint32_t* d_arrive = nullptr;  // [batch][kv_heads] arrival counters of the fused append
 };
 
 namespace kvq {
@@ -89,10 +92,14 @@ size_t append_smem(const kvq_cache* C);
 cudaError_t quant_setup(kvq_cache* C);
 cudaError_t decode_setup(kvq_cache* C);
 void* decode_kernel_fast(const kvq_cache* C);
+void* decode_kernel_fused(const kvq_cache* C);
 
 // decode: plans the split, launches the split-K kernel (which also combines)
 cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
                           cudaStream_t st, int* launches);
+
+cudaError_t launch_append_decode(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, const void* q,
+                                 int q_f32, float scale, float* out, cudaStream_t st, int* launches);
 
 cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,
                                   cudaStream_t st, int* launches, float* work, uint32_t* tickets);

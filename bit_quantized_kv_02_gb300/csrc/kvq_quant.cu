@@ -21,136 +21,7 @@
 
 namespace kvq {
 
-// ------------------------------------------------------- group statistics --
-
-// Warp-cooperative min / max / absmax over count values base[i*stride].
-__device__ __forceinline__ void warp_stats(const float* base, int count, int stride, float* mn, float* mx,
-                                           float* am) {
-  float a = INFINITY, b = -INFINITY, c = 0.0f;
-  for (int i = threadIdx.x & 31; i < count; i += 32) {
-    float v = base[(long)i * stride];
-    a = fminf(a, v);
-    b = fmaxf(b, v);
-    c = fmaxf(c, fabsf(v));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
-    c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
-  }
-  *mn = a;
-  *mx = b;
-  *am = c;
-}
-
-__device__ __forceinline__ float load_in(const void* p, long idx, int f32) {
-  return f32 ? reinterpret_cast<const float*>(p)[idx] : __half2float(reinterpret_cast<const __half*>(p)[idx]);
-}
-
-// Inverse of elem_pos: which (token, channel) of the tile a (lane, pair, half) holds.
-__device__ __forceinline__ void elem_of(int is_value, int lane, int pi, int e, int* t, int* c) {
-  int j = pi >> 2, r = pi & 3, rh = r & 1, kh = r >> 1;
-  int g = lane >> 2, tig = lane & 3;
-  int R = g + 8 * rh, kk = 2 * tig + 8 * kh + e;
-  if (is_value) {
-    *t = kk;
-    *c = 16 * j + R;
-  } else {
-    *t = R;
-    *c = 16 * j + kk;
-  }
-}
-
-// Value of tile word `wi` (0 .. D*bits/2-1) built from codes[t*D + c] (t < 16).
-__device__ __forceinline__ uint32_t build_word(const uint8_t* codes, int D, const Planes& pl, int is_value, int wi) {
-  // which plane
-  int p = 0;
-  for (int q = 1; q < pl.n; ++q)
-    if (wi >= D * pl.off[q] / 2) p = q;
-  int w = pl.w[p];
-  int W = D * w / 64, P = 16 / w;
-  int rel = wi - D * pl.off[p] / 2;
-  int lane = rel / W, i = rel % W;
-  uint32_t word = 0, mask = (1u << w) - 1u;
-  for (int k = 0; k < P; ++k) {
-    for (int e = 0; e < 2; ++e) {
-      int t, c;
-      elem_of(is_value, lane, i * P + k, e, &t, &c);
-      uint32_t code = codes[t * D + c];
-      word |= ((code >> pl.off[p]) & mask) << (k * w + 16 * e);
-    }
-  }
-  return word;
-}
-
-// Bits of tile word `wi` that belong to token row `trow`.
-__device__ __forceinline__ uint32_t word_token_mask(int D, const Planes& pl, int is_value, int wi, int trow) {
-  int p = 0;
-  for (int q = 1; q < pl.n; ++q)
-    if (wi >= D * pl.off[q] / 2) p = q;
-  int w = pl.w[p];
-  int W = D * w / 64, P = 16 / w;
-  int rel = wi - D * pl.off[p] / 2;
-  int lane = rel / W, i = rel % W;
-  uint32_t m = 0, mask = (1u << w) - 1u;
-  for (int k = 0; k < P; ++k)
-    for (int e = 0; e < 2; ++e) {
-      int t, c;
-      elem_of(is_value, lane, i * P + k, e, &t, &c);
-      if (t == trow) m |= mask << (k * w + 16 * e);
-    }
-  return m;
-}
-
-// Write the tile words of one 16-token tile (codes in shared memory, [16][D]).
-__device__ void store_tile(uint32_t* dst, const uint8_t* codes, int D, const TensorLayout& L, int is_value) {
-  int nw = L.tile_words;  // multiple of 32 (D*bits/2, D >= 64)
-  for (int q = threadIdx.x; q < nw / 4; q += blockDim.x) {
-    uint4 v;
-    v.x = build_word(codes, D, L.planes, is_value, 4 * q + 0);
-    v.y = build_word(codes, D, L.planes, is_value, 4 * q + 1);
-    v.z = build_word(codes, D, L.planes, is_value, 4 * q + 2);
-    v.w = build_word(codes, D, L.planes, is_value, 4 * q + 3);
-    reinterpret_cast<uint4*>(dst)[q] = v;
-  }
-}
-
-__device__ __forceinline__ void atomic_max_pos(uint32_t* addr, float v) {
-  // non-negative floats order like their bit patterns
-  if (v > 0.0f) atomicMax(addr, __float_as_uint(v));
-}
-
 // --------------------------------------------------------------- prefill ---
-
-struct QuantArgs {
-  TensorLayout L;
-  int is_value;
-  int layer, B, H, D, tcap, ntiles;
-  const void* x;  // [B][t_stride][H][D]
-  int x_f32;
-  long t_stride;
-  const int32_t* lens;  // device lens of this layer
-  char* base;           // cache buffer
-  uint32_t* smax;       // [B][H] for this tensor and layer
-};
-
-__device__ __forceinline__ uint32_t* codes_ptr(const QuantArgs& a, int b, int h, int tile) {
-  return reinterpret_cast<uint32_t*>(a.base + a.L.codes_off + a.layer * a.L.codes_layer) +
-         ((((long)b * a.H + h) * a.ntiles + tile) * a.L.tile_words);
-}
-__device__ __forceinline__ char* meta_ptr(const QuantArgs& a) {
-  return a.base + a.L.meta_off + a.layer * a.L.meta_layer;
-}
-__device__ __forceinline__ long bh_of(const QuantArgs& a, int b, int h) { return (long)b * a.H + h; }
-// fp16 rows of (b, h): ring of L.ring rows, token t at row t % ring
-__device__ __forceinline__ __half* tail_ptr(const QuantArgs& a, int b, int h) {
-  return reinterpret_cast<__half*>(a.base + a.L.tail_off + a.layer * a.L.tail_layer) +
-         (((long)b * a.H + h) * a.L.ring) * a.D;
-}
-__device__ __forceinline__ __half* tail_row(const QuantArgs& a, int b, int h, long t) {
-  return tail_ptr(a, b, h) + (t % a.L.ring) * a.D;
-}
 
 // Quantize a per-channel group block: G tokens x D channels of head h held in
 // shared memory as floats; writes the D metadata entries of group g and the
@@ -158,22 +29,27 @@ __device__ __forceinline__ __half* tail_row(const QuantArgs& a, int b, int h, lo
 __device__ void quant_channel_block(const QuantArgs& a, int b, int h, int g, const float* xs, uint8_t* cs,
                                     float* zs, float* ss) {
   const int G = a.L.group, D = a.D;
-  const int warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
   char* meta = meta_ptr(a);
   float smax_local = 0.0f;
-  for (int c = warp; c < D; c += nwarp) {
-    float mn, mx, am;
-    warp_stats(xs + c, G, D, &mn, &mx, &am);
+  // one thread per channel, reading the column in token order (consecutive
+  // threads, consecutive banks); min, max and absmax are exact in any order
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float mn = INFINITY, mx = -INFINITY, am = 0.0f;
+    for (int t = 0; t < G; ++t) {
+      const float v = xs[t * D + c];
+      mn = fminf(mn, v);
+      mx = fmaxf(mx, v);
+      am = fmaxf(am, fabsf(v));
+    }
     float z, s;
     group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
-    if ((threadIdx.x & 31) == 0) {
-      zs[c] = z;
-      ss[c] = s;
-      long gi = (((long)b * a.H + h) * (a.tcap / G) + g) * D + c;
-      store_meta(meta, gi, a.L.meta_f32, a.L.sym, z, s);
-      smax_local = fmaxf(smax_local, s);
-    }
+    zs[c] = z;
+    ss[c] = s;
+    store_meta(meta, (((long)b * a.H + h) * (a.tcap / G) + g) * D + c, a.L.meta_f32, a.L.sym, z, s);
+    smax_local = fmaxf(smax_local, s);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) smax_local = fmaxf(smax_local, __shfl_xor_sync(0xffffffffu, smax_local, o));
   __syncthreads();
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     int c = i % D;
@@ -317,96 +193,6 @@ __global__ void set_lens_kernel(int32_t* lens, int32_t* head_lens, LensArg la, i
 
 // ---------------------------------------------------------------- append ---
 
-struct AppendArgs {
-  QuantArgs k, v;       // x points at [B][H][D] new tokens (t_stride unused)
-  int32_t* lens;        // device lens of the layer
-  int32_t* head_lens;   // [B][H] per-head length counters of the layer
-  int warp_smem;        // per-warp scratch bytes for the per-token path
-};
-
-// One warp appends the new token of (b, h) (old length n) to one tensor: a
-// per-token tensor quantizes the token row now and merges its codes into the
-// tile words that hold that row; a per-channel tensor stores it in the fp16
-// tail and reports (returns true) when the tail just filled up, so that the
-// caller seals the group with the whole CTA.  xs / cs: per-warp shared scratch.
-__device__ bool append_warp(const QuantArgs& a, int b, int h, int n, float* xs, uint8_t* cs, float* zs, float* ss) {
-  const int lane = threadIdx.x & 31;
-  const int D = a.D;
-  const long xs_t = (long)a.H * D;
-  const int R = a.L.window;
-  if (a.L.axis == 1) {
-    // fp16 row; a group seals once all its tokens are older than the window
-    const int G = a.L.group;
-    __half* row = tail_row(a, b, h, n);
-    for (int c = lane; c < D; c += 32) row[c] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
-    const int old = n + 1 - R;
-    return old >= G && old % G == 0;
-  }
-  const int whole = a.L.whole;
-  const int nh = whole ? a.H : 1;
-  const int rowlen = nh * D;
-  if (R) {
-    // per-token tensor with a window: fp16 row now, its 16-token block is
-    // quantized once all of it is older than the window
-    for (int c = lane; c < rowlen; c += 32)
-      tail_row(a, b, h + c / D, n)[c % D] = __float2half_rn(load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32));
-    const int old = n + 1 - R;
-    return old >= kTile && old % kTile == 0;
-  }
-  const int G = whole ? rowlen : a.L.group;
-  const int gpr = rowlen / G;
-  for (int c = lane; c < rowlen; c += 32) xs[c] = load_in(a.x, (long)b * xs_t + (long)h * D + c, a.x_f32);
-  __syncwarp();
-  char* meta = meta_ptr(a);
-  float smax_local = 0.0f;
-  for (int j = 0; j < gpr; ++j) {
-    float mn, mx, am;
-    warp_stats(xs + j * G, G, 1, &mn, &mx, &am);
-    float z, s;
-    group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
-    smax_local = fmaxf(smax_local, s);
-    if (lane == 0) {
-      zs[j] = z;
-      ss[j] = s;
-      const long mi = whole ? ((long)b * a.tcap + n) : ((((long)b * a.H + h) * a.tcap + n) * gpr + j);
-      store_meta(meta, mi, a.L.meta_f32, a.L.sym, z, s);
-    }
-  }
-  __syncwarp();
-  for (int c = lane; c < rowlen; c += 32) cs[c] = (uint8_t)quant_code(xs[c], zs[c / G], ss[c / G], a.L.bits, a.L.sym);
-  __syncwarp();
-  // merge into the tile words that hold token row trow
-  const int trow = n & 15, tile = n >> 4;
-  const Planes& pl = a.L.planes;
-  if (trow == 0) {
-    // a tile's first token clears the whole tile (a shorter re-prefill can leave
-    // older codes behind), so that later tokens only OR their bits in
-    for (int hh = 0; hh < nh; ++hh) {
-      uint4* dst = reinterpret_cast<uint4*>(codes_ptr(a, b, h + hh, tile));
-      for (int q = lane; q < a.L.tile_words / 4; q += 32) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    __syncwarp();
-  }
-  // each lane ORs the bits of its channels' codes into the words that hold
-  // them (the token row's bits are zero: the tile was cleared at its first
-  // token), fire-and-forget with no read of the old words
-  for (int i = lane; i < rowlen; i += 32) {
-    const int hh = i / D, c = i - hh * D;
-    const uint32_t code = cs[i];
-    const FragPos f = elem_pos(a.is_value, trow, c);
-    uint32_t* dst = codes_ptr(a, b, h + hh, tile);
-    for (int p = 0; p < pl.n; ++p) {
-      const int w = pl.w[p], lw = w == 1 ? 0 : (w == 2 ? 1 : (w == 4 ? 2 : 3));
-      const int word = D * pl.off[p] / 2 + f.lane * (D >> (6 - lw)) + (f.pi >> (4 - lw));
-      const int bit = ((f.pi & ((16 >> lw) - 1)) << lw) + 16 * f.e;
-      const uint32_t v = ((code >> pl.off[p]) & ((1u << w) - 1u)) << bit;
-      if (v) atomicOr(dst + word, v);
-    }
-  }
-  if (lane == 0 && smax_local > 0.0f)
-    for (int hh = 0; hh < nh; ++hh) atomic_max_pos(a.smax + (long)b * a.H + h + hh, smax_local);
-  return false;
-}
 
 // One CTA of 128 threads per (sequence, kv head): warp 0 appends the key, warp 1
 // the value; a per-channel tensor whose tail just filled up is then sealed by
@@ -447,8 +233,9 @@ __global__ void append_kernel(const __grid_constant__ AppendArgs a) {
       uint8_t* cs = reinterpret_cast<uint8_t*>(xs + G * D);
       float* zs = reinterpret_cast<float*>(cs + G * D);
       float* ss = zs + D;
+      const int lgD = 31 - __clz(D);  // D is a power of two
       for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-        xs[i] = __half2float(tail_row(q, b, h, (long)g * G + i / D)[i % D]);
+        xs[i] = __half2float(tail_row(q, b, h, (long)g * G + (i >> lgD))[i & (D - 1)]);
       __syncthreads();
       quant_channel_block(q, b, h, g, xs, cs, zs, ss);
     } else {
@@ -733,14 +520,19 @@ cudaError_t launch_dequantize(kvq_cache* C, int layer, void* k_out, void* v_out,
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, cudaStream_t st,
-                          int* launches) {
+AppendArgs make_append_args(const kvq_cache* C, int layer, const void* k, const void* v, int x_f32) {
   AppendArgs a;
   a.k = make_args(C, 0, layer, k, x_f32, 1);
   a.v = make_args(C, 1, layer, v, x_f32, 1);
   a.lens = C->d_lens + (long)layer * C->cfg.batch;
   a.head_lens = C->d_head_lens + (long)layer * C->cfg.batch * C->cfg.kv_heads;
   a.warp_smem = append_warp_smem(C);
+  return a;
+}
+
+cudaError_t launch_append(kvq_cache* C, int layer, const void* k, const void* v, int x_f32, cudaStream_t st,
+                          int* launches) {
+  AppendArgs a = make_append_args(C, layer, k, v, x_f32);
   size_t sm = append_smem(C);
   void* args[] = {&a};
   cudaError_t e = launch_pdl(reinterpret_cast<const void*>(&append_kernel), dim3(C->cfg.batch, C->cfg.kv_heads),

@@ -58,7 +58,8 @@ EXPORTED = ["kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_pre
             "kvq_decode_attn", "kvq_export", "kvq_cache_tcap", "kvq_get_lens", "kvq_decode_traffic",
             "kvq_device_status", "kvq_last_launches", "kvq_status_string", "kvq_last_error",
             "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static", "kvq_set_decode_kernel",
-            "kvq_decode_kernel_specialized", "kvq_dequantize", "kvq_decode_attn_materialized"]
+            "kvq_decode_kernel_specialized", "kvq_dequantize", "kvq_decode_attn_materialized",
+            "kvq_append_decode_attn"]
 
 
 def lib():
@@ -77,6 +78,7 @@ def lib():
         L.kvq_prefill_quantize.argtypes = [P, I, P, P, I, P, ctypes.c_int64, P]
         L.kvq_append.argtypes = [P, I, P, P, I, P]
         L.kvq_decode_attn.argtypes = [P, I, P, I, ctypes.c_float, P, P]
+        L.kvq_append_decode_attn.argtypes = [P, I, P, P, I, P, I, ctypes.c_float, P, P]
         L.kvq_export.argtypes = [P, I, P, P, P, P, P, P, P, P]
         L.kvq_cache_tcap.argtypes = [P]
         L.kvq_cache_tcap.restype = I
@@ -204,6 +206,20 @@ class KVQCache:
             out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
         _check(lib().kvq_decode_attn(self.handle, layer, _ptr(q), _dtype_code(q), float(scale), _ptr(out),
                                      _stream(stream)), "kvq_decode_attn", self.handle)
+        return out
+
+    def kvq_append_decode_attn(self, layer: int, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                               out: torch.Tensor | None = None, scale: float = 0.0, stream=None) -> torch.Tensor:
+        """kvq_append then kvq_decode_attn on `layer`, in one launch where the
+        layout allows it: k_new, v_new [batch][kv_heads][head_dim]; q
+        [batch][q_heads][head_dim]; returns fp32 [batch][q_heads][head_dim]."""
+        assert k_new.is_contiguous() and v_new.is_contiguous() and k_new.dtype == v_new.dtype
+        assert q.is_contiguous()
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        _check(lib().kvq_append_decode_attn(self.handle, layer, _ptr(k_new), _ptr(v_new), _dtype_code(k_new),
+                                            _ptr(q), _dtype_code(q), float(scale), _ptr(out), _stream(stream)),
+               "kvq_append_decode_attn", self.handle)
         return out
 
     def kvq_decode_attn_static(self, layer: int, q: torch.Tensor, out: torch.Tensor | None = None,

@@ -161,6 +161,25 @@ kvq_status kvq_append(kvq_cache_t cache, int layer, const void* k_new, const voi
 kvq_status kvq_decode_attn(kvq_cache_t cache, int layer, const void* q, int q_dtype, float softmax_scale,
                            float* out, void* stream);
 
+/* kvq_append followed by kvq_decode_attn on the same layer, in one launch:
+ * same arguments as the two calls (k_new / v_new: device [batch][kv_heads]
+ * [head_dim] of in_dtype; q / out as for kvq_decode_attn), same resulting
+ * cache contents, lengths and output up to fp32 summation order.  This is one
+ * decode step of a layer as the pages describe it: the new token's key and
+ * value enter the cache (section "O Imposto dos Sistemas e Por Que Nao E um
+ * Detalhe" of "O Seu Cache KV Nao Tem um Problema de Bits. Tem um Problema de
+ * Geometria": per-channel groups keep new tokens in fp16 until G exist), then
+ * the query attends over every cached token.  Inside the launch the warp
+ * whose token range holds the new token writes it (and seals a per-channel
+ * group that just filled) before it reads its tiles; nothing else waits.
+ * Formats without a compile-time specialisation, layouts with a
+ * full-precision window or whole-vector groups, and k_new / v_new not 8-byte
+ * aligned run the two kernels back to back instead (same results);
+ * kvq_last_launches tells which (1 or 2).  All-or-nothing:
+ * KVQ_ERR_CAPACITY (nothing launched) if any sequence is full. */
+kvq_status kvq_append_decode_attn(kvq_cache_t cache, int layer, const void* k_new, const void* v_new, int in_dtype,
+                                  const void* q, int q_dtype, float softmax_scale, float* out, void* stream);
+
 /* kvq_decode_attn without scratch memory from the caller: identical inputs,
  * output and numerics, but the split-K partials and combine tickets live in a
  * 16 MiB array compiled into libkvq (static device memory, held by every GPU
@@ -265,7 +284,7 @@ int kvq_decode_kernel_specialized(kvq_cache_t cache);
 kvq_status kvq_refresh_lens(kvq_cache_t cache, void* stream);
 
 /* Number of kernel launches the last kvq_decode_attn / kvq_append /
- * kvq_prefill_quantize call on this handle issued. */
+ * kvq_append_decode_attn / kvq_prefill_quantize call on this handle issued. */
 int kvq_last_launches(kvq_cache_t cache);
 
 /* Human-readable name of a status code (static string). */

@@ -78,6 +78,7 @@ def test_capacity_and_buffer_checks(L):
     assert L.kvq_cache_create(ctypes.byref(cfg), None, b.alloc, None, ctypes.byref(h)) == 1
     assert L.kvq_decode_attn(None, 0, None, 0, 0.0, None, None) == 1
     assert L.kvq_append(None, 0, None, None, 0, None) == 1
+    assert L.kvq_append_decode_attn(None, 0, None, None, 0, None, 0, 0.0, None, None) == 1
 
 
 @pytest.mark.parametrize("window", [0, 64])
