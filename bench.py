@@ -476,8 +476,8 @@ def host_threads() -> int:
 def cpu_baseline(wl, seconds):
     """The oracle on every host core (the reported baseline) and on one thread."""
     nt = host_threads()
-    gbs1, desc1, per1 = cpu_oracle_sample(wl, seconds=seconds / 2, threads=1)
-    gbs, desc, _ = cpu_oracle_sample(wl, seconds=seconds / 2, max_samples=64 * nt, threads=nt)
+    gbs1, desc1, per1 = cpu_oracle_sample(wl, seconds=seconds / 2, max_samples=1 << 30, threads=1)
+    gbs, desc, _ = cpu_oracle_sample(wl, seconds=seconds / 2, max_samples=1 << 30, threads=nt)
     return ({"value": round(gbs, 4), "unit": "GB/s", "cores": nt, "kind": "oracle", "sample": desc,
              "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1, "sample": desc1}}, per1)
 
