@@ -83,25 +83,6 @@ __device__ __forceinline__ uint32_t build_word(const uint8_t* codes, int D, cons
   return build_word_f(D, pl, is_value, wi, [&](int t, int c) { return (uint32_t)codes[t * D + c]; });
 }
 
-// Bits of tile word `wi` that belong to token row `trow`.
-__device__ __forceinline__ uint32_t word_token_mask(int D, const Planes& pl, int is_value, int wi, int trow) {
-  int p = 0;
-  for (int q = 1; q < pl.n; ++q)
-    if (wi >= D * pl.off[q] / 2) p = q;
-  int w = pl.w[p];
-  int W = D * w / 64, P = 16 / w;
-  int rel = wi - D * pl.off[p] / 2;
-  int lane = rel / W, i = rel % W;
-  uint32_t m = 0, mask = (1u << w) - 1u;
-  for (int k = 0; k < P; ++k)
-    for (int e = 0; e < 2; ++e) {
-      int t, c;
-      elem_of(is_value, lane, i * P + k, e, &t, &c);
-      if (t == trow) m |= mask << (k * w + 16 * e);
-    }
-  return m;
-}
-
 // Write the tile words of one 16-token tile (codes in shared memory, [16][D]).
 __device__ inline void store_tile(uint32_t* dst, const uint8_t* codes, int D, const TensorLayout& L, int is_value) {
   int nw = L.tile_words;  // multiple of 32 (D*bits/2, D >= 64)
