@@ -71,3 +71,43 @@ def test_full_size_sampled_parity(name):
         got = out[b, h * rep:(h + 1) * rep]
         err = np.abs(got - ref).max(axis=-1) / np.abs(ref).max(axis=-1)
         assert err.max() <= TOL, (name, b, h, err.max())
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_full_size_fused_step_sampled_parity(name):
+    """One decode step of the benchmark's step graph at full size: the new
+    token's append fused into the decode launch (one launch), planned for the
+    capacity.  Sampled (sequence, kv head) outputs against the oracle's
+    quantization of the prefix plus the new token."""
+    wl = WORKLOADS[name]()
+    B, Hq, H, D = wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim
+    rep = Hq // H
+    cap = wl.max_tokens + 8
+    cfg = kvq.make_config(1, B, Hq, H, D, cap, wl.k, wl.v)
+    cache = kvq.KVQCache(cfg)
+    cache.kvq_set_decode_plan(cap)
+    k, v = wl.layer_kv(0, "cuda", T=wl.max_tokens)
+    cache.kvq_prefill_quantize(0, k, v, wl.lens)
+    kn, vn = wl.step_kv(0, 0, "cuda")
+    q = wl.layer_query(0, 1, "cuda")
+    scale = np.float32(1.0 / np.sqrt(D))
+    out = cache.kvq_append_decode_attn(0, kn, vn, q, scale=float(scale))
+    assert cache.kvq_last_launches() == 1
+    torch.cuda.synchronize()
+    assert cache.kvq_device_status() == 0
+    cache.kvq_refresh_lens()  # the device lengths, advanced inside the launch
+    assert cache.kvq_get_lens(0) == [int(x) + 1 for x in wl.lens]
+    out = out.cpu().numpy()
+    tcap = cache.tcap
+    samples = sorted({(0, 0), (B // 2, H - 1), (B - 1, H // 2)})
+    for b, h in samples:
+        n = int(wl.lens[b])
+        kx = torch.cat([k[b:b + 1, :n, h:h + 1, :], kn[b:b + 1, None, h:h + 1, :]], dim=1)
+        vx = torch.cat([v[b:b + 1, :n, h:h + 1, :], vn[b:b + 1, None, h:h + 1, :]], dim=1)
+        kh = _oracle_head(kx, 0, 0, n + 1, wl.k, tcap)
+        vh = _oracle_head(vx, 0, 0, n + 1, wl.v, tcap)
+        qs = q[b:b + 1, h * rep:(h + 1) * rep].float().cpu().numpy()
+        ref = oracle.attention(kh[None, None], vh[None, None], qs, np.array([n + 1], np.int32), scale)[0]
+        got = out[b, h * rep:(h + 1) * rep]
+        err = np.abs(got - ref).max(axis=-1) / np.abs(ref).max(axis=-1)
+        assert err.max() <= TOL, (name, b, h, err.max())
