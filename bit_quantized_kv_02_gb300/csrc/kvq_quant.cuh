@@ -287,18 +287,17 @@ template <int CPL>
 __device__ __forceinline__ float append_token_lanes(const QuantArgs& a, int b, int h, int n, const float* x) {
   const int lane = threadIdx.x & 31;
   const int D = CPL * 32, G = a.L.group, lpg = G / CPL;  // lanes per group (a power of two, <= 32)
-  float mn = x[0], mx = x[0], am = fabsf(x[0]);
+  float mn = x[0], mx = x[0];
 #pragma unroll
   for (int i = 1; i < CPL; ++i) {
     mn = fminf(mn, x[i]);
     mx = fmaxf(mx, x[i]);
-    am = fmaxf(am, fabsf(x[i]));
   }
   for (int o = lpg >> 1; o > 0; o >>= 1) {  // stays inside the aligned group of lpg lanes
     mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
     mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
   }
+  const float am = fmaxf(fabsf(mn), fabsf(mx));  // the largest magnitude is at an end of the range
   float z, s;
   group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
   const int gpr = D / G;
@@ -327,8 +326,9 @@ __device__ __forceinline__ float append_token_lanes(const QuantArgs& a, int b, i
       if (v) atomicOr(dst + word, v);
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, o));
+  // every lane of a group holds its step: the largest over the groups needs
+  // only the rounds across groups
+  for (int o = 16; o >= lpg; o >>= 1) s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, o));
   if (lane == 0) atomic_max_pos(a.smax + (long)b * a.H + h, s);
   return s;
 }
