@@ -217,33 +217,55 @@ __device__ inline bool append_warp(const QuantArgs& a, int b, int h, int n, floa
 // One warp seals per-channel group g of (b, h) from its G fp16 rows: the
 // same statistics, metadata and tile words as the CTA-wide seal (min, max
 // and absmax are exact in any order; each code is quant_code of the same
-// value).  Statistics come straight from the rows (lane c owns channels c,
-// c+32, ...); codes are packed tile by tile from 16 rows staged in scratch.
-// scratch: 2*D floats of group parameters + 16*D halves (40*D bytes, 16-byte
-// aligned).  Returns the group's largest step.
+// value).  Lane l owns the CPL = D/32 adjacent channels [l*CPL, l*CPL+CPL)
+// and reads its slice of four rows per step with vector loads; codes are
+// packed tile by tile from 16 rows staged in scratch.  scratch: 2*D floats
+// of group parameters + 16*D halves (40*D bytes, 16-byte aligned).  Returns
+// the group's largest step.
+template <int CPL>
 __device__ inline float seal_channel_warp(const QuantArgs& a, int b, int h, int g, unsigned char* scratch) {
   const int lane = threadIdx.x & 31;
-  const int G = a.L.group, D = a.D;
+  const int G = a.L.group, D = CPL * 32;
   float* zs = reinterpret_cast<float*>(scratch);
   float* ss = zs + D;
   __half* rows = reinterpret_cast<__half*>(ss + D);  // [16][D]
   char* meta = meta_ptr(a);
-  float smax_local = 0.0f;
   // ring row of the group's first token; the G rows follow it, wrapping once
-  const __half* ring0 = tail_ptr(a, b, h);
-  const int r0 = (g * G) % a.L.ring, ring = a.L.ring;
-  for (int c = lane; c < D; c += 32) {
-    float mn = INFINITY, mx = -INFINITY, am = 0.0f;
-    int r = r0;
-    for (int t = 0; t < G; ++t) {
-      const float x = __half2float(ring0[(long)r * D + c]);
+  const __half* ring0 = tail_ptr(a, b, h) + lane * CPL;
+  const int ring = a.L.ring;
+  int r = (g * G) % ring;
+  float mn[CPL], mx[CPL];
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    mn[i] = INFINITY;
+    mx[i] = -INFINITY;
+  }
+  for (int t = 0; t < G; t += 4) {  // G is a multiple of 16
+    __half2 v[4][CPL / 2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const __half2* src = reinterpret_cast<const __half2*>(ring0 + (long)r * D);
+#pragma unroll
+      for (int i = 0; i < CPL / 2; ++i) v[u][i] = src[i];
       r = r + 1 == ring ? 0 : r + 1;
-      mn = fminf(mn, x);
-      mx = fmaxf(mx, x);
-      am = fmaxf(am, fabsf(x));
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int i = 0; i < CPL / 2; ++i) {
+        const float2 f = __half22float2(v[u][i]);
+        mn[2 * i] = fminf(mn[2 * i], f.x);
+        mx[2 * i] = fmaxf(mx[2 * i], f.x);
+        mn[2 * i + 1] = fminf(mn[2 * i + 1], f.y);
+        mx[2 * i + 1] = fmaxf(mx[2 * i + 1], f.y);
+      }
+  }
+  float smax_local = 0.0f;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) {
+    const int c = lane * CPL + i;
     float z, s;
-    group_params(mn, mx, am, a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
+    group_params(mn[i], mx[i], fmaxf(fabsf(mn[i]), fabsf(mx[i])), a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
     zs[c] = z;
     ss[c] = s;
     store_meta(meta, (((long)b * a.H + h) * (a.tcap / G) + g) * D + c, a.L.meta_f32, a.L.sym, z, s);
@@ -383,7 +405,7 @@ __device__ __forceinline__ void fused_append_body(const AppendArgs& ap, int b, i
       for (int i = 0; i < CPL; i += 2) row[i / 2] = __halves2half2(__float2half_rn(x[i]), __float2half_rn(x[i + 1]));
       if (((n + 1) & (q.L.group - 1)) == 0) {
         __syncwarp();  // the new row is in the tail
-        st = seal_channel_warp(q, b, h, (n + 1) / q.L.group - 1, scratch);
+        st = seal_channel_warp<CPL>(q, b, h, (n + 1) / q.L.group - 1, scratch);
       }
     } else {
       st = append_token_lanes<CPL>(q, b, h, n, x);
