@@ -186,6 +186,29 @@ __device__ __forceinline__ void group_params(float mn, float mx, float amax, int
   }
 }
 
+// quant_code with the step's reciprocal r = __frcp_rn(s) given: the same code.
+// q0 = (x - z) * r differs from the IEEE quotient Q = fl((x - z) / s) by less
+// than 2^-13 whenever |Q| <= 512 (two roundings of 2^-24 relative each, plus
+// Q's own), so if q0 lies farther than 2^-12 from a half-integer both round to
+// the same integer; otherwise (ties included), or for a subnormal r, a huge
+// quotient or a NaN, the IEEE division decides.
+__device__ __forceinline__ int quant_code_r(float x, float z, float s, float r, int bits, int sym) {
+  if (s == 0.0f) return sym ? (1 << (bits - 1)) : 0;
+  const float num = sym ? x : __fsub_rn(x, z);
+  const float q0 = __fmul_rn(num, r);
+  const float aq = fabsf(q0);
+  const float fr = aq - floorf(aq);
+  float t = (aq <= 512.0f && r >= 0x1p-125f && fabsf(fr - 0.5f) > 0x1p-12f) ? rintf(q0) : rintf(__fdiv_rn(num, s));
+  if (!sym) {
+    const float levels = (float)((1 << bits) - 1);
+    t = fminf(fmaxf(t, 0.0f), levels);
+    return (int)t;
+  }
+  const float qmax = (float)((1 << (bits - 1)) - 1);
+  t = fminf(fmaxf(t, -qmax), qmax);
+  return (int)t + (1 << (bits - 1));
+}
+
 __device__ __forceinline__ int quant_code(float x, float z, float s, int bits, int sym) {
   if (s == 0.0f) return sym ? (1 << (bits - 1)) : 0;
   if (!sym) {

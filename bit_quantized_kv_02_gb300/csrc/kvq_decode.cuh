@@ -548,7 +548,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     else if (seal_k) prot = min(prot, n_old + 1 - kG);
     if (VAXIS == 0) prot = min(prot, n_old & ~(kTile - 1));
     else if (seal_v) prot = min(prot, n_old + 1 - vG);
-    const int need = (seal_k || seal_v) ? 40 * D : 0;
+    const int need = (seal_k || seal_v) ? fused_append_scratch(D, 1, 1) : 0;
     early = min(min(ns, max(0, (prot - w0) / kTile)), ns - (need + stage_bytes - 1) / stage_bytes);
   }
   issue_first(0, early);

@@ -82,10 +82,10 @@ struct DecodeArgs {
 };
 
 // Scratch bytes one warp needs for the fused append: a per-channel seal's
-// (2*D floats of group parameters + 16 rows of D halves); per-token tensors
+// (3*D floats of group parameters + 16 rows of D halves); per-token tensors
 // need none.
 __host__ __device__ constexpr int fused_append_scratch(int D, int k_axis, int v_axis) {
-  return (k_axis == 1 || v_axis == 1) ? 40 * D : 0;
+  return (k_axis == 1 || v_axis == 1) ? 44 * D : 0;
 }
 
 // Host: the append arguments of a layer (kvq_quant.cu).

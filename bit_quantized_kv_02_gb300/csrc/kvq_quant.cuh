@@ -219,16 +219,17 @@ __device__ inline bool append_warp(const QuantArgs& a, int b, int h, int n, floa
 // and absmax are exact in any order; each code is quant_code of the same
 // value).  Lane l owns the CPL = D/32 adjacent channels [l*CPL, l*CPL+CPL)
 // and reads its slice of four rows per step with vector loads; codes are
-// packed tile by tile from 16 rows staged in scratch.  scratch: 2*D floats
-// of group parameters + 16*D halves (40*D bytes, 16-byte aligned).  Returns
-// the group's largest step.
+// packed tile by tile from 16 rows staged in scratch.  scratch: 3*D floats
+// of group parameters (zero, step, step reciprocal) + 16*D halves (44*D
+// bytes, 16-byte aligned).  Returns the group's largest step.
 template <int CPL>
 __device__ inline float seal_channel_warp(const QuantArgs& a, int b, int h, int g, unsigned char* scratch) {
   const int lane = threadIdx.x & 31;
   const int G = a.L.group, D = CPL * 32;
   float* zs = reinterpret_cast<float*>(scratch);
   float* ss = zs + D;
-  __half* rows = reinterpret_cast<__half*>(ss + D);  // [16][D]
+  float* rs = ss + D;                                // step reciprocals
+  __half* rows = reinterpret_cast<__half*>(rs + D);  // [16][D]
   char* meta = meta_ptr(a);
   // ring row of the group's first token; the G rows follow it, wrapping once
   const __half* ring0 = tail_ptr(a, b, h) + lane * CPL;
@@ -268,6 +269,7 @@ __device__ inline float seal_channel_warp(const QuantArgs& a, int b, int h, int 
     group_params(mn[i], mx[i], fmaxf(fabsf(mn[i]), fabsf(mx[i])), a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
     zs[c] = z;
     ss[c] = s;
+    rs[c] = __frcp_rn(s);
     store_meta(meta, (((long)b * a.H + h) * (a.tcap / G) + g) * D + c, a.L.meta_f32, a.L.sym, z, s);
     smax_local = fmaxf(smax_local, s);
   }
@@ -282,7 +284,7 @@ __device__ inline float seal_channel_warp(const QuantArgs& a, int b, int h, int 
     }
     __syncwarp();
     auto code = [&](int t, int c) {
-      return (uint32_t)quant_code(__half2float(rows[t * D + c]), zs[c], ss[c], a.L.bits, a.L.sym);
+      return (uint32_t)quant_code_r(__half2float(rows[t * D + c]), zs[c], ss[c], rs[c], a.L.bits, a.L.sym);
     };
     uint4* dst = reinterpret_cast<uint4*>(codes_ptr(a, b, h, (int)(t0 / kTile)));
     for (int q = lane; q < a.L.tile_words / 4; q += 32) {
@@ -326,8 +328,9 @@ __device__ __forceinline__ float append_token_lanes(const QuantArgs& a, int b, i
   if ((lane & (lpg - 1)) == 0)
     store_meta(meta_ptr(a), (((long)b * a.H + h) * a.tcap + n) * gpr + lane / lpg, a.L.meta_f32, a.L.sym, z, s);
   uint32_t code[CPL];
+  const float rcp = __frcp_rn(s);
 #pragma unroll
-  for (int i = 0; i < CPL; ++i) code[i] = (uint32_t)quant_code(x[i], z, s, a.L.bits, a.L.sym);
+  for (int i = 0; i < CPL; ++i) code[i] = (uint32_t)quant_code_r(x[i], z, s, rcp, a.L.bits, a.L.sym);
   const int trow = n & 15, tile = n >> 4;
   uint32_t* dst = codes_ptr(a, b, h, tile);
   if (trow == 0) {
@@ -383,7 +386,7 @@ __device__ __forceinline__ void load_lane_row(const void* x, long off, int f32, 
 // group is sealed.  Only layouts without a full-precision window and without
 // whole-vector groups (each (b, h) then owns everything it writes).  Both new
 // rows come straight into registers, lane l holding channels [l*D/32,
-// (l+1)*D/32), loaded together.  scratch: the seal's (40*D bytes).
+// (l+1)*D/32), loaded together.  scratch: the seal's (44*D bytes).
 // *kstep / *vstep: the largest key / value step written (0 when none).
 template <int D>
 __device__ __forceinline__ void fused_append_body(const AppendArgs& ap, int b, int h, int n, unsigned char* scratch,

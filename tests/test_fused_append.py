@@ -197,3 +197,53 @@ def test_fused_append_graph_replay():
         if ea[key] is not None:
             assert torch.equal(ea[key], eb[key]), key
     assert eb["lens"].cpu().tolist() == [x + 45 for x in n0]
+
+
+def test_fused_append_near_half_integer_quotients():
+    """Appended per-token values whose quotients (x - zero) / step sit on and
+    around half-integers (offsets from 0 up to 1e-3, across the 2^-12 cutoff
+    below which the IEEE division decides the rounding): codes equal the
+    oracle's and the append kernel's bit for bit."""
+    import oracle
+
+    B, Hq, H, D, G = 2, 4, 4, 64, 32
+    wl = W("near_half", B, Hq, H, D, (4, 32, PC, ASYM), (4, G, PT, ASYM), torch.float32, seed=11)
+    n0, steps = 40, 40
+    T = n0 + steps
+    k, v = wl.layer_kv(0, "cpu", T=T)
+    v = v.clone()
+    rng = np.random.default_rng(11)
+    deltas = [0.0, 2**-22, -2**-22, 2**-14, -2**-14, 2**-13, -2**-13, 2**-12, -2**-12, 2**-11, -2**-11,
+              2**-9, -2**-9, 1e-3, -1e-3]
+    for t in range(n0, T):
+        for b in range(B):
+            for h in range(H):
+                row = np.zeros(D, np.float32)
+                for j in range(D // G):
+                    row[j * G + 1] = np.float32(rng.uniform(0.5, 8.0))  # each group spans [0, M]
+                meta = oracle.quantize_tensor(row.reshape(1, 1, 1, D), np.array([1], np.int32), 16, 4, G, PT)["meta"]
+                for j in range(D // G):
+                    z, s = float(meta[j][0]), float(meta[j][1])
+                    assert z == 0.0
+                    for i in range(2, G):
+                        kk = int(rng.integers(0, 13))
+                        row[j * G + i] = np.float32((kk + 0.5 + deltas[(i + t) % len(deltas)]) * s)
+                v[b, t, h] = torch.from_numpy(row)
+    a = make_cache(wl, max_tokens=T)
+    b_ = make_cache(wl, max_tokens=T)
+    for c in (a, b_):
+        c.kvq_prefill_quantize(0, k[:, :n0].contiguous().cuda(), v[:, :n0].contiguous().cuda(), [n0] * B)
+    q = wl.layer_query(0).cuda()
+    for t in range(n0, T):
+        kn, vn = k[:, t].contiguous().cuda(), v[:, t].contiguous().cuda()
+        a.kvq_append(0, kn, vn)
+        b_.kvq_append_decode_attn(0, kn, vn, q)
+        assert b_.kvq_last_launches() == 1
+    ea, eb = a.kvq_export(0), b_.kvq_export(0)
+    torch.cuda.synchronize()
+    for key in ("codes_k", "codes_v", "meta_k", "meta_v", "lens", "tail_k"):
+        assert torch.equal(ea[key], eb[key]), key
+    ov = oracle_tensor(v, [T] * B, b_.tcap, wl.v, False)
+    ok = oracle_tensor(k, [T] * B, b_.tcap, wl.k, False)
+    assert_export_equal(eb, ov, wl.v, "v")
+    assert_export_equal(eb, ok, wl.k, "k")
