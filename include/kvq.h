@@ -260,8 +260,9 @@ kvq_status kvq_device_status(kvq_cache_t cache, void* stream);
  * split-K launch as if every sequence held max(its length, plan_tokens) tokens
  * (CTAs past a sequence's real length do no work).  A launch planned this way
  * stays valid while the cache grows up to plan_tokens, which is what a CUDA
- * graph that captured kvq_append + kvq_decode_attn and is replayed step after
- * step needs.  0 (default) plans for the current lengths. */
+ * graph that captured kvq_append + kvq_decode_attn (or kvq_append_decode_attn)
+ * and is replayed step after step needs.  0 (default) plans for the current
+ * lengths. */
 kvq_status kvq_set_decode_plan(kvq_cache_t cache, int plan_tokens);
 
 /* Decode kernel choice, two bits.  Bit 0: 0 (default) uses a compile-time
