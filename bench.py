@@ -4,9 +4,14 @@ One step = for every layer of the workload: kvq_append_decode_attn, i.e. the
 append of one new token per sequence (quantize / stage / seal) and the split-K
 attention over the packed cache, in one launch (the format's fused decode
 specialisation; formats without one run kvq_append then kvq_decode_attn).
-The default workload is the GPT-2-small-shaped cache (12
-layers, batch 8, 12 heads, head_dim 64, 2048 cached tokens, fp16 N(0,1) with
-1% of key channels x10), K 4-bit per-channel G=32 / V 4-bit per-token G=32.
+The default workload is the Llama-2-13B-shaped MHA cache (40 layers, batch
+16, 40 heads, head_dim 128, 4096 + 17 cached tokens fp16, keys with 4 fixed
+outlier channels per head x15), K 2-bit per-channel G=32 / V 2-bit per-token
+G=32 with a 17-token fp16 key tail: the largest workload that fits one GPU.
+`--workload` takes any registered workload (every variant of the five
+configurations, bit_quantized_kv_02_gb300.synth.WORKLOADS), an alias, a group
+(gpt2_sweep, llama2_13b_axes, wide_gqa_all, all) or a comma-separated list;
+one JSON line is printed per workload.
 
 The step is captured once as a CUDA graph of the public calls (planned for the
 full capacity, so one graph stays valid as the cache grows) and replayed.
@@ -18,18 +23,20 @@ Between timed steps a 256 MB buffer is written to flush the 126 MB L2.
           device-to-device into the graph's input buffers inside the timed region)
   e2e   : same metric with the inputs copied from pinned host memory and the
           outputs copied back to pinned host memory inside the timed region
-  roofline : decode kernel alone; CUDA events recorded around every decode
-          launch inside the graph (on the launching stream)
+  roofline : decode kernel alone; CUDA events on the launching stream around a
+          graph of the step's decode launches.  `traffic` is null: the DRAM
+          byte counts come from separate ncu captures (see profiles/).
+`--phase prefill` times kvq_prefill_quantize instead (fp16 keys and values of
+every layer in HBM -> packed codes, metadata and fp16 tails): bytes = fp16
+input read + codes, metadata and tail written.
 Under torchrun each rank runs its own shard of sequences (weak scaling, no
 data-path collective); rank 0 prints the max-over-ranks time.
 """
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
-import re
 import subprocess
 import sys
 import time
@@ -46,33 +53,14 @@ from bit_quantized_kv_02_gb300 import kvq, synth  # noqa: E402
 
 METRIC = "decode-attn achieved HBM GB/s (% of peak) and cached tokens/s on 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
-# the sources of the plain decode kernel (the one the roofline times); the
-# fused append in kvq_quant.cuh is compiled into the FUSED instantiation only
-DECODE_SOURCES = ["kvq_decode.cuh", "kvq_decode.cu", "kvq_decode_args.h", "kvq_common.cuh", "kvq_decode_table.cuh"]
 
 
 def workload(name: str, tokens: int = 0) -> synth.Workload:
-    wl = _workload(name)
+    wl = synth.workload(name)
     if tokens:
         wl.lens = [min(int(x), tokens) for x in wl.lens]
         wl.name += f"_t{tokens}"
     return wl
-
-
-def _workload(name: str) -> synth.Workload:
-    if name == "gpt2_small":
-        return synth.gpt2_small(kbits=4, vbits=4, kgroup=32, vgroup=32, kaxis=synth.PC, vaxis=synth.PT)
-    if name == "gpt2_small_k6v4":
-        return synth.gpt2_small(kbits=6, vbits=4, kgroup=64, vgroup=64, kaxis=synth.PT, vaxis=synth.PT)
-    if name == "llama2_13b":
-        return synth.llama2_13b()
-    if name == "wide_gqa":
-        return synth.wide_gqa()
-    if name == "serving_mix":
-        return synth.serving_mix()
-    if name == "tiny":
-        return synth.tiny()
-    raise SystemExit(f"unknown workload {name}")
 
 
 def measured_peaks():
@@ -81,28 +69,6 @@ def measured_peaks():
         d = json.load(open(p))
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
-
-
-def decode_source_hash() -> str:
-    h = hashlib.sha256()
-    for f in DECODE_SOURCES:
-        h.update(open(os.path.join(ROOT, "bit_quantized_kv_02_gb300", "csrc", f), "rb").read())
-    return h.hexdigest()[:16]
-
-
-def ncu_traffic(workload_name: str):
-    """DRAM bytes per decode launch from the committed ncu summary of this
-    workload (profiles/decode_kernel_<--workload>.md), if it was taken on the
-    current decode kernel source (else None)."""
-    p = os.path.join(ROOT, "profiles", f"decode_kernel_{workload_name}.md")
-    if not os.path.exists(p):
-        return None
-    text = open(p).read()
-    m = re.search(r"decode_source_hash:\s*([0-9a-f]+)", text)
-    t = re.search(r"dram_bytes_per_launch_full:\s*([0-9.eE+]+)", text)
-    if not m or not t or m.group(1) != decode_source_hash():
-        return None
-    return float(t.group(1))
 
 
 class _Nvml:
@@ -222,10 +188,10 @@ class Clocks:
                 "reasons": reasons, "samples": len(sm), "source": self.source}
 
 
-def run_ours(args, rank, world):
+def run_ours(args, rank, world, name):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
-    wl = workload(args.workload, args.tokens)
+    wl = workload(name, args.tokens)
     # weak scaling: each rank owns `batch` sequences of its own (its shard of the job)
     B = wl.batch
     L = wl.layers
@@ -402,7 +368,7 @@ def run_ours(args, rank, world):
                        "l2": "256 MB buffer written before every timed step (L2 flushed)",
                        "parallelism": f"dp{world} (sequences sharded, no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(args.workload) if not (args.tokens or args.window) else None,
+                         "frac": round(achieved / peak, 4), "traffic": None,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                          else "fallback",
                          "kernel": "decode_kernel", "bytes_per_launch": round(dec_bytes_per_launch),
@@ -419,6 +385,128 @@ def run_ours(args, rank, world):
         if mat is not None:
             res["materialized"] = mat
     return res, wl
+
+
+def run_prefill(args, rank, world, name):
+    """kvq_prefill_quantize of every layer: fp16 keys and values resident in
+    HBM (a few distinct input buffers, each far larger than L2, cycled over
+    the layers) -> packed codes, metadata and fp16 tails."""
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    wl = workload(name, args.tokens)
+    B, L, H, D = wl.batch, wl.layers, wl.kv_heads, wl.head_dim
+    steps, warm = args.steps, args.warmup
+    cfg = kvq.make_config(L, B, wl.q_heads, H, D, wl.max_tokens, wl.k, wl.v)
+    cache = kvq.KVQCache(cfg, device=dev)
+    nin = min(L, 3)
+    inputs = [wl.layer_kv(l, dev, T=wl.max_tokens) for l in range(nin)]
+    bt = kvq.kvq_cache_bytes(cfg, wl.lens)
+    read = 2.0 * sum(wl.lens) * H * D * 2  # fp16 keys and values of every valid token
+    written = (bt.packed + bt.metadata + bt.tail) / L
+    per_call = read + written
+    stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+
+    def one_step():
+        nonlocal launches
+        launches = 0
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for l in range(L):
+                k, v = inputs[l % nin]
+                cache.kvq_prefill_quantize(l, k, v, wl.lens, stream=stream)
+                launches += cache.kvq_last_launches()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1)
+
+    for _ in range(warm):
+        one_step()
+    kdist.barrier()
+    clocks = Clocks(dev) if rank == 0 else None
+    t = 0.0
+    for _ in range(steps):
+        t += one_step()
+        if clocks:
+            clocks.poll()
+    clk = clocks.stop() if clocks else None
+    kdist.barrier()
+    # end to end: the layer's fp16 inputs copied from pinned host memory inside the timed region
+    k_host = [x.cpu().pin_memory() for x in inputs[0]]
+    kd, vd = torch.empty_like(inputs[0][0]), torch.empty_like(inputs[0][1])
+    e2e_layers = min(L, 4)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for l in range(e2e_layers):
+            kd.copy_(k_host[0], non_blocking=True)
+            vd.copy_(k_host[1], non_blocking=True)
+            cache.kvq_prefill_quantize(l, kd, vd, wl.lens, stream=stream)
+        e1.record(stream)
+    stream.synchronize()
+    t_e2e = e0.elapsed_time(e1)
+    t_max = kdist.max_over_ranks(t, device=dev)
+    peak, peak_kind = measured_peaks()
+    res = None
+    if rank == 0:
+        value = per_call * L * steps * world / (t_max * 1e-3) / 1e9
+        achieved = per_call * L * steps / (t * 1e-3) / 1e9
+        res = {
+            "metric": "prefill quantize-and-pack achieved HBM GB/s (% of peak) on 1 GB300", "phase": "prefill",
+            "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps, "warmup": warm,
+            "ms_per_step": round(t_max / steps, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp16 in, 2..8-bit codes + fp16 metadata out", "data": "synthetic",
+            "pct_of_peak": round(100.0 * value / peak, 2),
+            "tokens_per_s": round(sum(wl.lens) * L * steps * world / (t_max * 1e-3), 1),
+            "config": {"workload": wl.name, "layers": L, "batch_per_gpu": B, "kv_heads": H, "head_dim": D,
+                       "cached_tokens": wl.lens[0], "k": list(wl.k), "v": list(wl.v),
+                       "step": "kvq_prefill_quantize of every layer (inputs cycled over "
+                               f"{nin} resident buffers of {2 * B * wl.max_tokens * H * D * 2 / 1e9:.2f} GB)",
+                       "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                         else "fallback",
+                         "kernel": "kvq_prefill_quantize (prefill_channel_kernel / prefill_token_kernel per tensor)",
+                         "bytes_per_launch": round(per_call), "read_bytes": round(read),
+                         "written_bytes": round(written), "us_per_call": round(t / (steps * L) * 1e3, 3)},
+            "gpu_launches": launches * steps,
+            "e2e": {"value": round(per_call * e2e_layers / (t_e2e * 1e-3) / 1e9, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": 2 * inputs[0][0].numel() * 2 * e2e_layers, "d2h_bytes_per_step": 0,
+                    "layers": e2e_layers, "path": "pinned host -> device copy of the layer's keys and values, "
+                                                  "kvq_prefill_quantize"},
+            "clocks": clk,
+        }
+    return res, wl
+
+
+def cpu_quantize_sample(wl, seconds=5.0):
+    """The oracle's quantizer on one (layer, sequence) sample, repeated for
+    about `seconds`: GB/s of the prefill path's algorithmic bytes."""
+    import oracle
+
+    D, H = wl.head_dim, wl.kv_heads
+    n = wl.lens[0]
+    k, v = wl.layer_kv(0, "cpu", T=n)
+    k, v = k[:1].float().numpy(), v[:1].float().numpy()
+    lens = np.array([n], np.int32)
+    pk, mk, tk = oracle.tensor_bytes(1, H, D, lens, wl.k[0], wl.k[1], wl.k[2], bool(wl.k[3]))
+    pv, mv, tv = oracle.tensor_bytes(1, H, D, lens, wl.v[0], wl.v[1], wl.v[2], bool(wl.v[3]))
+    sample_bytes = 2.0 * n * H * D * 2 + pk + mk + tk + pv + mv + tv
+    t0 = time.perf_counter()
+    count = 0
+    while True:
+        oracle.quantize_tensor(k, lens, n + (-n) % 128, *wl.k[:3], sym=bool(wl.k[3]))
+        oracle.quantize_tensor(v, lens, n + (-n) % 128, *wl.v[:3], sym=bool(wl.v[3]))
+        count += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(sample_bytes * count / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{count} x (one layer, one sequence: {n} tokens x {H} kv heads x {D}; quantize keys and "
+                      f"values), 1 thread, {el:.1f} s"}
 
 
 def cpu_oracle_sample(wl, seconds=10.0, max_samples=64, threads=1):
@@ -491,7 +579,9 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="gpt2_small")
+    ap.add_argument("--workload", default="llama2_13b",
+                    help="registered workload, alias, group or comma-separated list (one JSON line each)")
+    ap.add_argument("--phase", default="decode", choices=["decode", "prefill"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--tokens", type=int, default=0, help="cap the cached tokens per sequence (profiling runs)")
     ap.add_argument("--window", type=int, default=0,
@@ -506,7 +596,7 @@ def main():
         # the reference arm is the CPU oracle; under torchrun only rank 0 works
         if rank != 0:
             return
-        wl = workload(args.workload, args.tokens)
+        wl = workload(synth.workload_names(args.workload)[0], args.tokens)
         import oracle
         oracle.build()
         cb, per = cpu_baseline(wl, seconds=max(2.0, min(40.0, args.cpu_seconds * (args.steps + args.warmup) / 25)))
@@ -523,16 +613,23 @@ def main():
     kvq.lib()
     if world > 1:
         kdist.init("nccl")
-    res, wl = run_ours(args, rank, world)
-    if rank == 0:
-        import oracle
-        oracle.build()
-        res["cpu_baseline"], _ = cpu_baseline(wl, seconds=args.cpu_seconds)
-        print(json.dumps(res))
+    for name in synth.workload_names(args.workload):
+        if args.phase == "prefill":
+            res, wl = run_prefill(args, rank, world, name)
+        else:
+            res, wl = run_ours(args, rank, world, name)
+        if rank == 0:
+            import oracle
+            oracle.build()
+            if args.phase == "prefill":
+                res["cpu_baseline"] = cpu_quantize_sample(wl, seconds=args.cpu_seconds)
+            else:
+                res["cpu_baseline"], _ = cpu_baseline(wl, seconds=args.cpu_seconds)
+            print(json.dumps(res), flush=True)
+        torch.cuda.empty_cache()
     if world > 1:
         kdist.barrier()
         torch.distributed.destroy_process_group()
-
 
 if __name__ == "__main__":
     main()

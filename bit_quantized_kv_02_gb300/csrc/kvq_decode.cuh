@@ -400,16 +400,28 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     if (lane * 128 < row_bytes) prefetch_l2(static_cast<const char*>(a.ap.k.x) + xo + lane * 128);
     if (lane * 128 < row_bytes) prefetch_l2(static_cast<const char*>(a.ap.v.x) + xo + lane * 128);
   }
-  const int n_old = FUSED ? a.ap.head_lens[(long)b * H + h] : 0;
+  // fused append: one thread reads the old length and hands it to the whole
+  // CTA through shared memory, so no thread of the CTA reads the counter after
+  // the CTA has counted itself in below
+  __shared__ int s_n_old;
+  if (FUSED) {
+    if (threadIdx.x == 0) s_n_old = a.ap.head_lens[(long)b * H + h];
+    __syncthreads();
+  }
+  const int n_old = FUSED ? s_n_old : 0;
   const int n = FUSED ? n_old + 1 : a.lens[b];
   const int nchunks = (n + S - 1) / S;
-  // every CTA of (b, h) counts itself in once it has its old length (the
-  // length is consumed first: the count cannot pass the read); the last one
-  // advances the lengths, which no CTA of this launch reads afterwards
+  // every CTA of (b, h) counts itself in once its length read is complete (a
+  // fence orders the read before the count); the last one to arrive advances
+  // the lengths, which no CTA of this launch reads afterwards
   unsigned arrival = 0u;
-  if (FUSED && threadIdx.x == 0 && nchunks > 0) arrival = atomicAdd(a.arrive + (long)b * H + h, 1u);
+  if (FUSED && threadIdx.x == 0 && nchunks > 0) {
+    __threadfence();
+    arrival = atomicAdd(a.arrive + (long)b * H + h, 1u);
+  }
   auto advance_lengths = [&]() {
     if (FUSED && threadIdx.x == 0 && arrival == gridDim.x - 1u) {
+      __threadfence();  // every other CTA's read precedes its count, which precedes this write
       a.ap.head_lens[(long)b * H + h] = n;
       if (h == 0) a.ap.lens[b] = n;
       a.arrive[(long)b * H + h] = 0u;

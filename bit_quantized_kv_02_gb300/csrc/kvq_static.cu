@@ -51,6 +51,7 @@ extern "C" kvq_status kvq_decode_attn_static(kvq_cache_t C, int layer, const voi
   if (!C || layer < 0 || layer >= C->cfg.layers) return KVQ_ERR_INVALID_ARG;
   if (!q || !out || (q_dtype != KVQ_F16 && q_dtype != KVQ_F32)) return KVQ_ERR_INVALID_ARG;
   if (!(softmax_scale > 0.0f)) softmax_scale = 1.0f / std::sqrt((float)C->cfg.head_dim);
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   const kvq_config& c = C->cfg;
   const size_t work_bytes = align256(kvq::decode_work_floats(c.batch, c.q_heads, c.head_dim, C->max_chunks) * 4);
   const size_t ticket_bytes = kvq::decode_ticket_words(c.batch, c.kv_heads, C->max_chunks) * 4;
@@ -70,7 +71,10 @@ extern "C" kvq_status kvq_decode_attn_static(kvq_cache_t C, int layer, const voi
   float* work = static_cast<float*>(base);
   uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(base) + work_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // the tickets must start at zero; the array keeps whatever the last call left
+  // The tickets must start at zero.  A completed call leaves them at zero
+  // (the merging CTA resets each ticket it used), but the array keeps whatever
+  // the last call left, and a call that did not complete (a launch that failed
+  // or was aborted) can leave counts behind: clear them on every call.
   e = cudaMemsetAsync(tickets, 0, ticket_bytes, st);
   C->last_launches = 0;
   if (e == cudaSuccess)

@@ -185,7 +185,7 @@ def llama2_13b(kaxis=PC, vaxis=PT, seed=0, batch=16, sealed=4096, tail=17, layer
     """Llama-2-13B-shaped MHA cache: 40 layers, 40 KV heads, head_dim 128,
     batch 16, 4096 + 17 tokens fp16; keys with 4 fixed outlier channels per
     head x15, values N(0,1); 2-bit G=32."""
-    return Workload(f"llama2_13b_{'kc' if kaxis else 'kt'}{'vc' if vaxis else 'vt'}", layers, batch, 40, 40, 128,
+    return Workload(f"llama2_13b_{'kc' if kaxis else 'kt'}_{'vc' if vaxis else 'vt'}", layers, batch, 40, 40, 128,
                     [sealed + tail] * batch, (2, 32, kaxis, ASYM), (2, 32, vaxis, ASYM), torch.float16,
                     key_outliers_per_head=4, key_outlier_scale=15.0, seed=seed)
 
@@ -210,3 +210,82 @@ def serving_mix(seed=0, batch=64, lo=1024, hi=32768) -> Workload:
     G=64, V 2-bit per-token G=64."""
     return Workload("serving_mix", 1, batch, 32, 8, 128, ragged_lengths(batch, lo, hi, seed * 1000 + 77),
                     (2, 64, PC, ASYM), (2, 64, PT, ASYM), torch.float16, value_dist="laplace", seed=seed)
+
+
+# ------------------------------------------------------------ registry ----
+
+GPT2_BITS = (2, 3, 4, 6, 8)
+GPT2_GROUPS = (32, 64, WHOLE)
+
+
+def _gname(g):
+    return "whole" if g == WHOLE else str(g)
+
+
+def gpt2_variant(kbits, vbits, group, reading, layers=12) -> Workload:
+    """One setting of the GPT-2-small bits x group sweep.  reading "pt": keys
+    and values both grouped per token along channels (groups of 32 or 64
+    channels of a head, or the whole 768-channel token vector); reading "pc":
+    keys grouped per channel along `group` tokens (128 tokens for the "whole"
+    column, the largest per-channel group), values per token along channels as
+    in "pt"."""
+    if reading == "pt":
+        kc, vc = (kbits, group, PT), (vbits, group, PT)
+    else:
+        kc, vc = (kbits, 128 if group == WHOLE else group, PC), (vbits, group, PT)
+    wl = gpt2_small(kbits=kbits, vbits=vbits, kgroup=kc[1], vgroup=vc[1], kaxis=kc[2], vaxis=vc[2], layers=layers)
+    wl.name = f"gpt2_small_k{kbits}v{vbits}_g{_gname(group)}_{reading}"
+    return wl
+
+
+def _registry():
+    reg = {"tiny": lambda layers=None: tiny()}
+    for rd in ("pt", "pc"):
+        for b in GPT2_BITS:
+            for g in GPT2_GROUPS:
+                reg[f"gpt2_small_k{b}v{b}_g{_gname(g)}_{rd}"] = (
+                    lambda layers=None, b=b, g=g, rd=rd: gpt2_variant(b, b, g, rd, layers or 12))
+        for kb, vb in ((6, 4), (4, 6)):
+            reg[f"gpt2_small_k{kb}v{vb}_g64_{rd}"] = (
+                lambda layers=None, kb=kb, vb=vb, rd=rd: gpt2_variant(kb, vb, 64, rd, layers or 12))
+    for ka in (PC, PT):
+        for va in (PT, PC):
+            name = f"llama2_13b_{'kc' if ka else 'kt'}_{'vc' if va else 'vt'}"
+            reg[name] = lambda layers=None, ka=ka, va=va: llama2_13b(kaxis=ka, vaxis=va, layers=layers or 40)
+    for var in ("k4v8", "sym6"):
+        for ka in (PT, PC):
+            reg[f"wide_gqa_{var}_{'kc' if ka else 'kt'}"] = lambda layers=None, var=var, ka=ka: wide_gqa(var, ka)
+    reg["serving_mix"] = lambda layers=None: serving_mix()
+    return reg
+
+
+WORKLOADS = _registry()
+# short names of the headline setting of each workload
+ALIASES = {"gpt2_small": "gpt2_small_k4v4_g32_pc", "gpt2_small_k6v4": "gpt2_small_k6v4_g64_pt",
+           "llama2_13b": "llama2_13b_kc_vt", "wide_gqa": "wide_gqa_k4v8_kt"}
+GROUPS = {
+    "gpt2_sweep": [n for n in WORKLOADS if n.startswith("gpt2_small")],
+    "llama2_13b_axes": [n for n in WORKLOADS if n.startswith("llama2_13b")],
+    "wide_gqa_all": [n for n in WORKLOADS if n.startswith("wide_gqa")],
+}
+GROUPS["all"] = [n for n in WORKLOADS if n != "tiny"]
+
+
+def workload(name: str, layers=None) -> Workload:
+    """A registered workload by name (or alias), optionally with fewer layers."""
+    name = ALIASES.get(name, name)
+    if name not in WORKLOADS:
+        raise KeyError(f"unknown workload {name}")
+    return WORKLOADS[name](layers)
+
+
+def workload_names(spec: str) -> list:
+    """Names of a comma-separated list of workloads, aliases or groups."""
+    out = []
+    for part in spec.split(","):
+        part = part.strip()
+        if part in GROUPS:
+            out += GROUPS[part]
+        elif part:
+            out.append(ALIASES.get(part, part))
+    return out

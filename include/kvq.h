@@ -195,9 +195,13 @@ kvq_status kvq_append_decode_attn(kvq_cache_t cache, int layer, const void* k_ne
  *  - The first call on a device looks up the array's device address with that
  *    device current (cudaGetSymbolAddress); make that first call before any
  *    stream capture.
- *  - Every call shares the one array and finds the last call's contents in it:
- *    the tickets are cleared at each call, and calls that overlap on the GPU
- *    (different streams, handles or threads) race with each other. */
+ *  - Every call shares the one array and finds the last call's contents in it.
+ *    The combine tickets are cleared on `stream` at each call (one memset
+ *    before the launch): a completed call leaves them at zero, but a call whose
+ *    launch failed or was aborted may not.  Calls that overlap on the GPU
+ *    (different streams, handles or threads) race with each other.
+ *  - Argument checks are those of kvq_decode_attn (KVQ_ERR_INVALID_ARG for a bad
+ *    layer, a null pointer, an unknown dtype or a non-finite softmax_scale). */
 kvq_status kvq_decode_attn_static(kvq_cache_t cache, int layer, const void* q, int q_dtype, float softmax_scale,
                                   float* out, void* stream);
 

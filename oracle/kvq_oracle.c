@@ -30,7 +30,7 @@
  *  - "Whole vector" groups: "Asymetrie kvantizace KV cache", section "Vychozi
  *    zjisteni na GPT-2" (scaling over the whole vector vs per head).
  *
- * Readings where the pages are silent (all documented in the design notes):
+ * Readings where the pages are silent, taken as follows:
  *  - ties round half to even (rintf in the default rounding mode);
  *  - metadata stored as fp16: zero rounded toward -inf, step rounded toward +inf,
  *    step recomputed from the stored zero, so every input lies in
