@@ -81,6 +81,7 @@ def _load():
         lib.kvqo_attention.argtypes = [P, P, P, P, I, I, I, I, I, F, P]
         lib.kvqo_attention.restype = I
         lib.kvqo_tensor_bytes.argtypes = [I, I, I, P, I, I, I, I, I, I, P]
+        lib.kvqo_rope.argtypes = [P, I, I, I, I, P, ctypes.c_double]
         lib.kvqo_cache_elements.argtypes = [I, ctypes.c_double, I, I]
         lib.kvqo_cache_elements.restype = ctypes.c_double
         _lib = lib
@@ -198,6 +199,16 @@ def attention(khat, vhat, q, lens, scale: float) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle: bad head counts")
     return out
+
+
+def rope(x, lens, base: float) -> np.ndarray:
+    """Rotary position embedding of [B][H][T][D] float64 rows (row t = the token
+    at position t), rows t < lens[b]; returns a rotated copy."""
+    x = np.array(x, dtype=np.float64, order="C", copy=True)
+    lens = np.ascontiguousarray(lens, dtype=np.int32)
+    batch, heads, tcap, dim = x.shape
+    _load().kvqo_rope(_ptr(x), batch, heads, dim, tcap, _ptr(lens), float(base))
+    return x
 
 
 def tensor_bytes(batch, heads, dim, lens, bits, group, axis, sym=False, meta_f32=False, window=0):

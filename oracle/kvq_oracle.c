@@ -398,6 +398,37 @@ int kvqo_attention(const double* khat, const double* vhat, const float* q, const
   return 0;
 }
 
+/* ------------------------------------------------------------- RoPE ------ */
+
+/* Rotary position embedding applied to dequantized keys ("O Seu Cache KV Nao
+ * Tem um Problema de Bits. Tem um Problema de Geometria", section "Embebedos
+ * Rotatorios Complicam as Chaves": RoPE turns pairs of channels by an angle
+ * set by the token's position, which spreads a fixed outlier channel into its
+ * neighbour; the remedy there is to quantize keys before the rotation and to
+ * rotate after dequantization; section "O Que Fazer Com Isso", item 2).
+ * Readings where the page is silent: the pairs are adjacent channels
+ * (2i, 2i+1); pair i of the token at position t turns by t * theta_i with
+ * theta_i = base^(-2i/dim); a token's position is its index in the sequence.
+ *   (x0, x1) -> (x0 cos a - x1 sin a, x0 sin a + x1 cos a),  a = t * theta_i.
+ * In place on x [batch][heads][tcap][dim] (fp64), rows t < lens[b]. */
+void kvqo_rope(double* x, int batch, int heads, int dim, int tcap, const int* lens, double base) {
+  for (int b = 0; b < batch; ++b) {
+    for (int h = 0; h < heads; ++h) {
+      for (long t = 0; t < lens[b]; ++t) {
+        double* row = x + (((long)b * heads + h) * tcap + t) * dim;
+        for (int i = 0; i < dim / 2; ++i) {
+          double theta = pow(base, -2.0 * (double)i / (double)dim);
+          double a = (double)t * theta;
+          double c = cos(a), sn = sin(a);
+          double x0 = row[2 * i], x1 = row[2 * i + 1];
+          row[2 * i] = x0 * c - x1 * sn;
+          row[2 * i + 1] = x0 * sn + x1 * c;
+        }
+      }
+    }
+  }
+}
+
 /* ------------------------------------------------------------ sizes ------ */
 
 /* Bytes of one layer-tensor holding lens[b] tokens, split into the terms of
