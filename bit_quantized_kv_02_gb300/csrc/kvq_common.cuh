@@ -67,6 +67,20 @@ __host__ __device__ inline Planes planes_of(int bits) {
   return p;
 }
 
+// The same plane split as compile-time functions of the bit width: plane
+// count, width of plane p, bit offset of plane p.
+__host__ __device__ constexpr int np_of(int b) { return (b == 3 || b == 5 || b == 6) ? 2 : (b == 7 ? 3 : 1); }
+__host__ __device__ constexpr int pw_of(int b, int p) {
+  return b == 2   ? 2
+         : b == 3 ? (p == 0 ? 2 : 1)
+         : b == 4 ? 4
+         : b == 5 ? (p == 0 ? 4 : 1)
+         : b == 6 ? (p == 0 ? 4 : 2)
+         : b == 7 ? (p == 0 ? 4 : (p == 1 ? 2 : 1))
+                  : 8;
+}
+__host__ __device__ constexpr int po_of(int b, int p) { return p == 0 ? 0 : pw_of(b, 0) + (p == 2 ? pw_of(b, 1) : 0); }
+
 // Position of one element inside the fragment-ordered tile.
 struct FragPos {
   int lane;

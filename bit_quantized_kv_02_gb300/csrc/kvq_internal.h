@@ -88,6 +88,12 @@ cudaError_t launch_export(kvq_cache* C, int layer, int is_value, uint8_t* codes,
                           cudaStream_t st);
 size_t append_smem(const kvq_cache* C);
 
+// fast prefill kernels (kvq_prefill.cu): fp16 inputs, no window, no whole-vector groups
+struct QuantArgs;
+bool prefill_fast_ok(const QuantArgs& a);
+cudaError_t launch_prefill_fast(const QuantArgs& a, int maxn, cudaStream_t st);
+cudaError_t prefill_fast_setup();
+
 // one-time kernel attribute set-up at cache creation (keeps launches capturable)
 cudaError_t quant_setup(kvq_cache* C);
 cudaError_t decode_setup(kvq_cache* C);

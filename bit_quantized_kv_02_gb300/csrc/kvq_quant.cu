@@ -465,7 +465,10 @@ cudaError_t launch_prefill(kvq_cache* C, int layer, const void* k, const void* v
   for (int is_v = 0; is_v < 2; ++is_v) {
     QuantArgs a = make_args(C, is_v, layer, is_v ? v : k, x_f32, t_stride);
     if (maxn == 0) continue;
-    if (a.L.axis == 1) {
+    if (prefill_fast_ok(a)) {
+      cudaError_t e = launch_prefill_fast(a, maxn, st);
+      if (e != cudaSuccess) return e;
+    } else if (a.L.axis == 1) {
       size_t sm = channel_smem(a.L.group, D);
       dim3 grid((maxn + a.L.group - 1) / a.L.group + 1, H, B);
       prefill_channel_kernel<<<grid, 256, sm, st>>>(a);
@@ -562,6 +565,7 @@ cudaError_t quant_setup(kvq_cache* C) {
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)append_smem(C));
   if (e == cudaSuccess) e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess) e = prefill_fast_setup();
   return e;
 }
 

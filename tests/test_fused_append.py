@@ -137,15 +137,19 @@ def test_fused_append_planned_ahead_multi_wave():
     assert run_steps(wl, n0, 33, plan_tokens=4000, check_every=16) == {1}
 
 
+@pytest.mark.parametrize("fmt", ["mha_g32", "gqa4_g64"])
 @pytest.mark.parametrize("bits", [0, 2], ids=["cluster_or_global", "global_combine"])
-def test_fused_append_ragged_dead_chunks_many_steps(bits):
+def test_fused_append_ragged_dead_chunks_many_steps(bits, fmt):
     """Ragged lengths (empty, one token, thousands) under a launch planned far
     beyond them: most CTAs of each (sequence, head) lie past its end and count
     themselves in as soon as they start, racing the CTAs that still hold work.
     Every CTA reads the old length before any CTA of its (sequence, head) can
     advance it, so over many steps the lengths, the cache and the outputs stay
     exactly those of the separate calls and the oracle."""
-    wl = W("ragged_dead", 6, 8, 4, 128, (2, 32, PC, ASYM), (2, 32, PT, ASYM), torch.float16, seed=12)
+    if fmt == "mha_g32":  # formats with a fused specialisation (one launch per step)
+        wl = W("ragged_dead", 6, 4, 4, 128, (2, 32, PC, ASYM), (2, 32, PT, ASYM), torch.float16, seed=12)
+    else:
+        wl = W("ragged_dead", 6, 8, 2, 128, (2, 64, PC, ASYM), (2, 64, PT, ASYM), torch.float16, seed=12)
     n0 = [2500, 40, 0, 700, 1, 129]
     assert run_steps(wl, n0, 64, fused_kernel_bits=bits, plan_tokens=6000, check_every=16) == {1}
 
