@@ -58,6 +58,9 @@ kvq_status validate(const kvq_config* c) {
       return KVQ_ERR_UNSUPPORTED;
   }
   if ((long)c->max_tokens > (1L << 30)) return KVQ_ERR_UNSUPPORTED;
+  if (!std::isfinite(c->rope_theta) || c->rope_theta < 0.0f || (c->rope_theta > 0.0f && c->rope_theta <= 1.0f))
+    return KVQ_ERR_INVALID_ARG;
+  if (c->rope_theta > 0.0f && c->max_tokens > (1 << 24)) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 

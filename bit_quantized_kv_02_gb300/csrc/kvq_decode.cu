@@ -41,6 +41,13 @@ static bool cluster_fits(const void* fn, size_t smem, int rep, int D, int occ, i
   return occ2 >= std::min(occ, 4);
 }
 
+void* pick_kernel_rope(int D, bool r8, int vaxis) {
+  if (D == 64) return decode_kernel_ptr_rope_d64(r8, vaxis);
+  if (D == 128) return decode_kernel_ptr_rope_d128(r8, vaxis);
+  if (D == 256) return decode_kernel_ptr_rope_d256(r8, vaxis);
+  return nullptr;
+}
+
 void* pick_kernel(int D, bool r8, int vaxis) {
   if (D == 64) return decode_kernel_ptr_d64(r8, vaxis);
   if (D == 128) return decode_kernel_ptr_d128(r8, vaxis);
@@ -101,8 +108,11 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   // global memory, prefetched into L2 when their tile is issued
   a.stage_f16 = 0;
   a.arrive = C->d_arrive;
+  const int rope = cfg.rope_theta > 0.0f;
+  a.rope_l2b = rope ? std::log2((double)cfg.rope_theta) : 0.0;
   const DecLayout L = dec_layout(D, rep, C->k.bits, C->k.axis, C->k.whole, C->k.gpt, C->k.meta_bytes, C->v.bits,
-                                 C->v.axis, C->v.whole, C->v.gpt, C->v.meta_bytes, 0);
+                                 C->v.axis, C->v.whole, C->v.gpt, C->v.meta_bytes, 0, rope);
+  a.rope_off = L.rope_off;
   a.st_kc = L.st_kc;
   a.st_km = L.st_km;
   a.st_vc = L.st_vc;
@@ -122,7 +132,10 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
 }
 
 cudaError_t decode_setup(kvq_cache* C) {
-  void* fn = C->generic_decode ? nullptr : decode_kernel_fast(C);
+  // pre-RoPE caches run the rotary instances of the runtime-format kernel
+  const bool rope = C->cfg.rope_theta > 0.0f;
+  void* fn = (C->generic_decode || rope) ? nullptr : decode_kernel_fast(C);
+  if (!fn && rope) fn = pick_kernel_rope(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
   if (!fn) fn = pick_kernel(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
   if (!fn) return cudaErrorInvalidValue;
   C->dec_fn = fn;
@@ -149,7 +162,7 @@ cudaError_t decode_setup(kvq_cache* C) {
   // residency and cluster merge (the launch is planned for the plain kernel)
   const int ring = (1 << P.a.lg_nstages) * P.a.stage_bytes;
   C->fused_ok = 0;
-  C->dec_fn_fused = C->generic_decode ? nullptr : decode_kernel_fused(C);
+  C->dec_fn_fused = (C->generic_decode || rope) ? nullptr : decode_kernel_fused(C);
   if (C->dec_fn_fused && C->k.window == 0 && C->v.window == 0 && !C->k.whole && !C->v.whole &&
       fused_append_scratch(C->cfg.head_dim, C->k.axis, C->v.axis) <= ring) {
     void* ff = C->dec_fn_fused;
@@ -297,7 +310,8 @@ cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16,
                                        int q_f32, float scale, float* out, cudaStream_t st, int* launches) {
   const kvq_config& cfg = C->cfg;
   const int D = cfg.head_dim, rep = cfg.q_heads / cfg.kv_heads;
-  void* fn = pick_kernel(D, rep == 8, 1);
+  const int rope = cfg.rope_theta > 0.0f;  // the rows hold pre-RoPE keys: rotate them as the fused path does
+  void* fn = rope ? pick_kernel_rope(D, rep == 8, 1) : pick_kernel(D, rep == 8, 1);
   if (!fn) return cudaErrorInvalidValue;
   Plan P;
   int occ_unused = 1;
@@ -317,7 +331,8 @@ cudaError_t launch_decode_materialized(kvq_cache* C, int layer, const void* k16,
   tail_only(a.K, k16);
   tail_only(a.V, v16);
   a.stage_f16 = 1;
-  const DecLayout L = dec_layout(D, rep, a.K.bits, 1, 0, 0, a.K.meta_bytes, a.V.bits, 1, 0, 0, a.V.meta_bytes, 1);
+  const DecLayout L = dec_layout(D, rep, a.K.bits, 1, 0, 0, a.K.meta_bytes, a.V.bits, 1, 0, 0, a.V.meta_bytes, 1, rope);
+  a.rope_off = L.rope_off;
   a.st_kc = L.st_kc;
   a.st_km = L.st_km;
   a.st_vc = L.st_vc;

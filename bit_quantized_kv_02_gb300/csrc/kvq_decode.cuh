@@ -42,20 +42,6 @@
 
 namespace kvq {
 
-// ---------------------------------------------------------------- planes ---
-
-__host__ __device__ constexpr int np_of(int b) { return (b == 3 || b == 5 || b == 6) ? 2 : (b == 7 ? 3 : 1); }
-__host__ __device__ constexpr int pw_of(int b, int p) {
-  return b == 2   ? 2
-         : b == 3 ? (p == 0 ? 2 : 1)
-         : b == 4 ? 4
-         : b == 5 ? (p == 0 ? 4 : 1)
-         : b == 6 ? (p == 0 ? 4 : 2)
-         : b == 7 ? (p == 0 ? 4 : (p == 1 ? 2 : 1))
-                  : 8;
-}
-__host__ __device__ constexpr int po_of(int b, int p) { return p == 0 ? 0 : pw_of(b, 0) + (p == 2 ? pw_of(b, 1) : 0); }
-
 // Code-to-operand conversion.  Widths 2, 4 and 8 place each code, unshifted
 // or after one shift shared by several registers, in the low mantissa bits of
 // an fp16 subnormal: the register's value is code * 2^(base - 24), exact, with
@@ -135,18 +121,29 @@ __device__ __forceinline__ void convert_dispatch(int bits, const uint32_t* tile,
 // upper fragment half (hsel > 0: entries i >= hsel, i.e. tokens 8..15 of a
 // per-token tile; hsel <= 0: channels with bit 3 set), else post_lo.  One
 // warp, entries strided over the lanes.
+// center (per-token values): the codes enter the MMA centred on the middle of
+// their range (code - 2^(B-1), see the value kernel's centring MMA), so the
+// zero point becomes zero + 2^(B-1) * step (symmetric: exactly 0).
 __device__ __forceinline__ void canon_meta(const char* src, int n, int bits, int sym, int meta_f32, float post_lo,
-                                           float post_hi, int hsel, float2* dst, int lane) {
+                                           float post_hi, int hsel, float2* dst, int lane, bool center = false) {
   const float off = (float)conv_off(bits);
   const float soff = (float)(1 << (bits - 1));
   for (int i = lane; i < n; i += 32) {
     float z, s;
     load_meta(src, i, meta_f32, sym, &z, &s);
-    if (sym) z = -s * soff;
+    float zc;
+    if (center) zc = sym ? 0.0f : fmaf(soff, s, z);
+    else zc = (sym ? -s * soff : z) - off * s;
     const bool hi = hsel > 0 ? (i >= hsel) : ((i & 8) != 0);
-    dst[i] = make_float2(s * (hi ? post_hi : post_lo), z - off * s);
+    dst[i] = make_float2(s * (hi ? post_hi : post_lo), zc);
   }
 }
+
+// Probabilities enter the value MMAs, the row sums and the split-K partials
+// as p * 2^kPExp (p <= 1): a probability of a long, flat softmax (1e-5 and
+// below) then stays a normal fp16 in both halves of its hi + lo split instead
+// of losing its low half to fp16 subnormals.  The scale cancels in out = O / l.
+constexpr float kPExp = 14.0f;
 
 template <bool R8>
 struct Slots {
@@ -360,7 +357,10 @@ __host__ __device__ constexpr int decode_min_blocks(int D, bool is_static) {
 
 // FUSED: the launch also appends the new token (kvq_append_decode_attn); the
 // plain decode kernel is compiled without any of that code.
-template <int D, bool R8, int VAXIS, class CFG, bool FUSED = false>
+// ROPE: the keys are cached before the rotary position embedding; every
+// dequantized key is turned by its token's angles before the QK MMA (runtime
+// formats only).
+template <int D, bool R8, int VAXIS, class CFG, bool FUSED = false, bool ROPE = false>
 __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages != 0)) decode_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NCH = D / 16;                // 16-channel chunks / m-tiles
@@ -570,7 +570,27 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     const int i = threadIdx.x + u * 128;
     if (i < rep * D) qs[i] = qv[u] * a.scale_log2;
   }
+  // rotary tables: pair frequencies theta_i = base^(-2i/D) as fp32 (hi, lo)
+  // pairs from one fp64 evaluation each; then (cos, sin)(u * theta_i) for the
+  // sixteen token offsets u of a tile
+  float2* rth = reinterpret_cast<float2*>(smem + a.rope_off);  // [D/2]
+  float2* rtab = rth + D / 2;                                   // [16][rope_row(D)]
+  float2* rbase = rtab + 16 * rope_row(D) + warp * (D / 2);     // this warp's tile bases [D/2]
+  if (ROPE && threadIdx.x < D / 2) {
+    const double th = exp2(-(2.0 * threadIdx.x / D) * a.rope_l2b);
+    const float hi = (float)th;
+    rth[threadIdx.x] = make_float2(hi, (float)(th - (double)hi));
+  }
   __syncthreads();
+  if (ROPE) {
+    for (int i = threadIdx.x; i < 16 * (D / 2); i += blockDim.x) {
+      const int u = i / (D / 2), pr = i - u * (D / 2);
+      const float2 th = rth[pr];
+      float sn, cs;
+      sincosf(fmaf((float)u, th.x, (float)u * th.y), &sn, &cs);
+      rtab[u * rope_row(D) + pr] = make_float2(cs, sn);
+    }
+  }
   if (k_token) {
     const int Gk = kwhole ? D : kG;  // within one head a whole-vector group spans all D channels
     for (int i = threadIdx.x; i < kgpt * rep; i += blockDim.x) {
@@ -654,13 +674,38 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const float k_chi = exp2i(-conv_c(kbits));
   const int v_cg = conv_g(vbits), v_cr = conv_r(vbits);
   const float v_chi = exp2i(-conv_c(vbits));
-  if (k_token) {
+  // Per-token values of 3, 5, 6, 7 and 8 bits: a second MMA per chunk with a
+  // constant A of -(conv_off + 2^(B-1)) (in each register's conversion scale)
+  // and the tile's P operand centres the codes on their mid-range inside the
+  // accumulator, so O never holds the large offset sum (up to 1.5 * 2^B steps
+  // per token) that the zero points would cancel later (fp32 cancellation
+  // over long ranges); the zero points carry the matching + 2^(B-1) * step.
+  // Every constant is an exact fp16.  2- and 4-bit codes enter with no offset
+  // and a mid-range of at most 7.5 steps: measured, the extra MMA and its
+  // registers cost more there (9 % on a 2-bit head_dim 128 batch) than the
+  // accuracy it adds.
+  const bool vcen = VAXIS == 0 && vbits != 2 && vbits != 4;
+  uint32_t acen[4];
+  {
+    const float cen = (float)(conv_off(vbits) + (1 << (vbits - 1)));
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const __half hv = __float2half_rn(-cen * exp2i(v_cg + v_cr * (r & 1) + conv_c(vbits) * (r >> 1)));
+      acen[r] = pack_h2(hv, hv);
+    }
+  }
+  if (ROPE) {
+    // dequantized, rotated keys meet the plain query
+    build_qb<D, R8>(qs, rep, nullptr, kbits, ksym, kf32, barea, wbias, E_unit, 1.0f, lane);
+    qb_state = 1;
+    load_b();
+  } else if (k_token) {
     build_qb<D, R8>(qs, rep, nullptr, kbits, ksym, kf32, barea, wbias, E_unit, k_chi, lane);
     qb_state = 0;
     load_b();
   }
-  // value step normalisation: every folded p * step lies below 2^15
-  const int E_v = VAXIS == 0 ? norm_exp(smax_v) : 0;
+  // value step normalisation: every folded p * step (p scaled by 2^kPExp) lies below 2^15
+  const int E_v = VAXIS == 0 ? norm_exp(smax_v) - (int)kPExp : 0;
   const float sc_v = exp2i(E_v), inv_sc_v = exp2i(-E_v);
   const int hl = g & 1;
   // per-lane rows into the canonical metadata
@@ -750,7 +795,32 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     const bool vflush = VAXIS == 1 && vp && ((t0 + kTile) & vgmask) == 0;
 
     // ---- metadata of this stage -> canonical fp32 pairs
-    if (kp) {
+    if (ROPE) {
+      // keys: (step, zero') per channel of the group (at its first tile) or
+      // per (token, group), in plain units; the register scales are applied
+      // when each register is dequantized
+      if (kp && (k_token || (t0 & kgmask) == 0))
+        canon_meta(reinterpret_cast<const char*>(st + st_km), k_token ? kTile * gs_k : D, kbits, ksym, kf32, 1.0f,
+                   1.0f, 8 * gs_k, canK, lane);
+      // this tile's angle bases (cos, sin)(t0 * theta_i), halved (the rotated
+      // keys enter the MMA at half scale so they stay inside fp16's range).
+      // Exact two-term reduction of t0 * theta_i modulo 2 pi (Cody and Waite's
+      // additive reduction with FMA): t0 < 2^24 is exact, the product's error is
+      // recovered with an FMA, 2 pi is split in its nearest float and the rest.
+      const float tf = (float)t0;
+      for (int pr = lane; pr < D / 2; pr += 32) {
+        const float2 th = rth[pr];
+        const float p0 = tf * th.x;
+        const float pe = fmaf(tf, th.x, -p0);
+        const float kq = rintf(p0 * 0.159154943091895335769f);
+        float r = fmaf(-kq, 6.28318548202514648438f, p0);
+        r = fmaf(-kq, -1.74845553146951715e-7f, r);
+        r += pe + tf * th.y;
+        float sn, cs;
+        __sincosf(r, &sn, &cs);
+        rbase[pr] = make_float2(0.5f * cs, 0.5f * sn);
+      }
+    } else if (kp) {
       if (k_token) {
         if (qb_state != 0) {
           Ek = E_unit;
@@ -777,7 +847,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     if (vp) {
       if (VAXIS == 0)
         canon_meta(reinterpret_cast<const char*>(st + st_vm), kTile * gs_v, vbits, vsym, vf32, sc_v, sc_v * v_chi,
-                   8 * gs_v, canV, lane);
+                   8 * gs_v, canV, lane, vcen);
       else if (vflush)
         canon_meta(reinterpret_cast<const char*>(st + st_vm), D, vbits, vsym, vf32, exp2i(-v_cg), exp2i(-v_cg - v_cr), 0,
                    canV, lane);
@@ -843,7 +913,95 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           if (ktok && ((j + 1) & (cpgk - 1)) == 0) fold(j >> lg_cpgk);
         }
       };
-      if (kp) {
+      if constexpr (ROPE) {
+        // Dequantize each key register (row token g + 8 rh, channel pair
+        // i = 8j + tig + 4 kh: the two halves are the pair's channels), turn it
+        // by the token's angle t * theta_i = (t0 + u) * theta_i with
+        // cos/sin(t0 theta + u theta) from this tile's bases and the in-tile
+        // table, and feed it as an fp16 hi + lo pair against the plain query.
+        auto rope_chunk = [&](int j, const uint32_t* A, bool packed, int kb) {
+          uint32_t Ah[4], Al[4];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int rh = r & 1, kh = r >> 1;
+            const int pr = 8 * j + tig + 4 * kh, c0 = 2 * pr;
+            float2 x = __half22float2(*reinterpret_cast<const __half2*>(&A[r]));
+            if (packed) {
+              const float us = exp2i(-(conv_g(kb) + conv_r(kb) * rh + conv_c(kb) * kh));
+              if (k_token) {
+                const float2 m = canK[(g + 8 * rh) * gs_k + (kwhole ? 0 : (c0 >> k_lgG))];
+                x.x = fmaf(x.x * us, m.x, m.y);
+                x.y = fmaf(x.y * us, m.x, m.y);
+              } else {
+                const float4 m = *reinterpret_cast<const float4*>(canK + c0);
+                x.x = fmaf(x.x * us, m.x, m.y);
+                x.y = fmaf(x.y * us, m.z, m.w);
+              }
+            }
+            const float2 bs = rbase[pr], ut = rtab[(g + 8 * rh) * rope_row(D) + pr];
+            const float cs = bs.x * ut.x - bs.y * ut.y, sn = bs.y * ut.x + bs.x * ut.y;
+            const float r0 = cs * x.x - sn * x.y, r1 = sn * x.x + cs * x.y;
+            const __half2 hh = __floats2half2_rn(r0, r1);
+            const float2 hf = __half22float2(hh);
+            const __half2 ll = __floats2half2_rn(r0 - hf.x, r1 - hf.y);
+            Ah[r] = *reinterpret_cast<const uint32_t*>(&hh);
+            Al[r] = *reinterpret_cast<const uint32_t*>(&ll);
+          }
+#pragma unroll
+          for (int hl2 = 0; hl2 < NB; ++hl2) {
+            uint32_t b0, b1;
+            if (BREG) {
+              b0 = breg[BREG ? (j * NB + hl2) * 2 : 0];
+              b1 = breg[BREG ? (j * NB + hl2) * 2 + 1 : 0];
+            } else {
+              const uint2 v = reinterpret_cast<const uint2*>(barea)[(j * NB + hl2) * 32 + lane];
+              b0 = v.x;
+              b1 = v.y;
+            }
+            mma_16816(C, Ah[0], Ah[1], Ah[2], Ah[3], b0, b1);
+            mma_16816(C2, Al[0], Al[1], Al[2], Al[3], b0, b1);
+          }
+        };
+        auto rope_packed = [&](auto kb) {
+          constexpr int KB = decltype(kb)::value;
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            uint32_t A[4];
+            convert_chunk<KB, D>(ktile, lane, j, A);
+            rope_chunk(j, A, true, KB);
+          }
+        };
+        if (kp) {
+          switch (kbits) {
+            case 2: rope_packed(IntC<2>{}); break;
+            case 3: rope_packed(IntC<3>{}); break;
+            case 4: rope_packed(IntC<4>{}); break;
+            case 5: rope_packed(IntC<5>{}); break;
+            case 6: rope_packed(IntC<6>{}); break;
+            case 7: rope_packed(IntC<7>{}); break;
+            default: rope_packed(IntC<8>{}); break;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            const __half* tb = (f16st ? reinterpret_cast<const __half*>(st + st_kc) : ktail + (long)(t0 % kring) * D) +
+                               16 * j + 2 * tig;
+            uint32_t A[4];
+            A[0] = *reinterpret_cast<const uint32_t*>(tb + (long)g * D);
+            A[1] = *reinterpret_cast<const uint32_t*>(tb + (long)(g + 8) * D);
+            A[2] = *reinterpret_cast<const uint32_t*>(tb + (long)g * D + 8);
+            A[3] = *reinterpret_cast<const uint32_t*>(tb + (long)(g + 8) * D + 8);
+            rope_chunk(j, A, false, 16);
+          }
+        }
+        // keys at half scale, query at 2^E_unit
+        const float inv = exp2i(1 - E_unit);
+#pragma unroll
+        for (int q = 0; q < SL::N; ++q) {
+          const float v = R8 ? (C[q] + C2[q]) : (C[2 * q] + C[2 * q + 1] + C2[2 * q] + C2[2 * q + 1]);
+          score[q] += v * inv;
+        }
+      } else if (kp) {
         switch (kbits) {
           case 2: qk_packed(IntC<2>{}); break;
           case 3: qk_packed(IntC<3>{}); break;
@@ -867,7 +1025,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           mma_chunk(j, A);
         }
       }
-      if (!ktok) fold(0);
+      if (!ROPE && !ktok) fold(0);
     }
 
     // --------------------------------------------------------- softmax --
@@ -910,7 +1068,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       }
 #pragma unroll
       for (int q = 0; q < SL::N; ++q) {
-        p[q] = fast_exp2(score[q] - m_run[q]);
+        p[q] = fast_exp2(score[q] - m_run[q] + kPExp);
         l_run[q] = l_run[q] * alpha[q] + p[q];
       }
     }
@@ -1027,6 +1185,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           uint32_t A[4];
           convert_chunk<VB, D>(vtile, lane, j, A);
           mma_v(j, A, true);
+          if (VAXIS == 0 && vcen) mma_v(j, acen, true);
         }
       };
       if (vp) {

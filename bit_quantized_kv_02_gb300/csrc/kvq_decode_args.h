@@ -73,6 +73,8 @@ struct DecodeArgs {
   int stage_off;            // offset of the stage ring inside the per-warp region
   int head_bytes;           // CTA head region (q, group sums)
   int stage_f16;            // fp16 rows (window, unsealed groups) are staged through the ring too
+  double rope_l2b;          // log2 of the rotary embedding's base (the kernel's ROPE instantiation)
+  int rope_off;             // byte offset of the rotary tables inside the CTA head region
   // fused append (the kernel's FUSED instantiation, kvq_append_decode_attn):
   // the warp whose range holds the new token appends it first; lengths come
   // from ap.head_lens (old length + 1) and the last CTA of each (sequence,
@@ -98,7 +100,14 @@ struct DecLayout {
   int st_kc, st_km, st_vc, st_vm;              // offsets inside a stage
   int stage_bytes, lg_ns;                      // stage size, log2 of the stage count
   int barea_bytes, canon_k, canon_v, stage_off, warp_bytes, head_bytes;
+  int rope_off;                                // rotary tables inside the head region (rope layouts)
 };
+
+// Rotary tables of a decode CTA (floats2): the pair frequencies theta_i as
+// (hi, lo) [D/2], the in-tile turns (cos, sin)(u * theta_i) [16][D/2 + 4]
+// (rows padded against bank conflicts), and each warp's per-tile bases [4][D/2].
+__host__ __device__ constexpr int rope_row(int D) { return D / 2 + 4; }
+__host__ __device__ constexpr int rope_bytes(int D) { return (D / 2 + 16 * rope_row(D) + 4 * (D / 2)) * 8; }
 
 __host__ __device__ constexpr int dl_round(int x, int m) { return (x + m - 1) / m * m; }
 __host__ __device__ constexpr int dl_max(int x, int y) { return x > y ? x : y; }
@@ -106,7 +115,7 @@ __host__ __device__ constexpr int dl_max(int x, int y) { return x > y ? x : y; }
 // f16: stage slots also hold a 16-token tile of fp16 rows (32 * D bytes per tensor)
 __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, int kaxis, int kwhole, int kgpt,
                                                    int kmb, int vbits, int vaxis, int vwhole, int vgpt, int vmb,
-                                                   int f16 = 0) {
+                                                   int f16 = 0, int rope = 0) {
   DecLayout L{};
   L.kc_bytes = D * kbits * 2;
   L.vc_bytes = D * vbits * 2;
@@ -121,13 +130,15 @@ __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, in
   L.stage_bytes = dl_round(L.st_vm + L.vm_bytes, 128);
   L.lg_ns = L.stage_bytes <= 4096 ? 2 : 1;
   L.barea_bytes = (D / 16) * 32 * 8 * (rep == 8 ? 2 : 1);
-  L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : 0;  // per-channel keys are read from the stage
+  // per-channel keys are read from the stage, except by the rotary kernel, which keeps the group's D entries
+  L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : (rope ? D : 0);
   L.canon_v = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) : D;
   L.stage_off = dl_round(L.barea_bytes + (L.canon_k + L.canon_v) * 8 + 32, 128);
   L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns), 128);
   const int merge_bytes = 4 * rep * (D + 2) * 4;
   if (L.warp_bytes * 4 < merge_bytes) L.warp_bytes = dl_round((merge_bytes + 3) / 4, 128);
-  L.head_bytes = dl_round((rep * D + (kaxis == 0 ? kgpt * rep : 0)) * 4, 128);
+  L.rope_off = dl_round((rep * D + (kaxis == 0 ? kgpt * rep : 0)) * 4, 16);
+  L.head_bytes = dl_round(L.rope_off + (rope ? rope_bytes(D) : 0), 128);
   return L;
 }
 
@@ -135,6 +146,10 @@ __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, in
 void* decode_kernel_ptr_d64(bool r8, int vaxis);
 void* decode_kernel_ptr_d128(bool r8, int vaxis);
 void* decode_kernel_ptr_d256(bool r8, int vaxis);
+// the same with the rotary embedding of the keys (pre-RoPE caches)
+void* decode_kernel_ptr_rope_d64(bool r8, int vaxis);
+void* decode_kernel_ptr_rope_d128(bool r8, int vaxis);
+void* decode_kernel_ptr_rope_d256(bool r8, int vaxis);
 
 // compile-time specialisation for this cache's formats, or null (generic kernel)
 void* decode_kernel_fast(const kvq_cache* C);

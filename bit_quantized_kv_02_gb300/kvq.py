@@ -42,7 +42,7 @@ class Config(ctypes.Structure):
     _fields_ = [("layers", ctypes.c_int), ("batch", ctypes.c_int), ("q_heads", ctypes.c_int),
                 ("kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("max_tokens", ctypes.c_int),
                 ("k", TensorCfg), ("v", TensorCfg), ("meta_dtype", ctypes.c_int), ("max_splits", ctypes.c_int),
-                ("recent_window", ctypes.c_int)]
+                ("recent_window", ctypes.c_int), ("rope_theta", ctypes.c_float)]
 
 
 class Bytes(ctypes.Structure):
@@ -109,15 +109,17 @@ def lib():
 
 
 def make_config(layers, batch, q_heads, kv_heads, head_dim, max_tokens, k, v, meta_dtype=F16, max_splits=0,
-                recent_window=0):
+                recent_window=0, rope_theta=0.0):
     """k, v: (bits, group, axis, mode) tuples or dicts; recent_window: fp16 window
-    of the newest tokens of both tensors (multiple of 16, 0 = none)."""
+    of the newest tokens of both tensors (multiple of 16, 0 = none); rope_theta:
+    base of the rotary embedding applied to the dequantized keys at decode (keys
+    cached before RoPE; 0 = none)."""
     def tc(t):
         if isinstance(t, dict):
             return TensorCfg(t["bits"], t["group"], t["axis"], t.get("mode", ASYM))
         return TensorCfg(*t)
     return Config(layers, batch, q_heads, kv_heads, head_dim, max_tokens, tc(k), tc(v), meta_dtype, max_splits,
-                  recent_window)
+                  recent_window, float(rope_theta))
 
 
 def _check(st: int, what: str, handle=None):

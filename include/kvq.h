@@ -98,6 +98,14 @@ typedef struct {
                         R, a per-token tensor quantizes a 16-token block once all of it is older than the
                         newest R (from the tokens' fp16 values); the newer tokens are held in fp16.  With
                         R = 0 per-token tensors quantize every token on arrival. */
+  float rope_theta; /* 0 = keys are cached and attended as given.  > 0: pre-RoPE key quantization ("O Seu
+                       Cache KV Nao Tem um Problema de Bits...", sections "Embebedos Rotatorios Complicam
+                       as Chaves" and "O Que Fazer Com Isso", item 2): the caller passes keys BEFORE the
+                       rotary position embedding, they are quantized as given, and decode attention turns
+                       every dequantized key of token t (its index in the sequence) by the embedding:
+                       channel pair (2i, 2i+1) by the angle t * rope_theta^(-2i/head_dim).  The query is
+                       passed as the model rotates it (post-RoPE).  Finite, 0 or > 1; positions below
+                       2^24. */
 } kvq_config;
 
 /* Byte accounting.  The first four terms follow the memory model total =

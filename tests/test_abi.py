@@ -46,7 +46,7 @@ def _cfg(**kw):
     base.update(kw)
     return kvq.make_config(base["layers"], base["batch"], base["q_heads"], base["kv_heads"], base["head_dim"],
                            base["max_tokens"], base["k"], base["v"], base.get("meta_dtype", 0), base.get("max_splits", 0),
-                           base.get("recent_window", 0))
+                           base.get("recent_window", 0), base.get("rope_theta", 0.0))
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -56,6 +56,8 @@ def _cfg(**kw):
     (dict(k=(4, 32, 2, 0)), 1), (dict(k=(4, 32, 1, 5)), 1), (dict(meta_dtype=3), 1), (dict(layers=0), 1),
     (dict(kv_heads=16, head_dim=256, v=(4, -1, 0, 0), q_heads=16), 2),
     (dict(recent_window=8), 1), (dict(recent_window=-16), 1), (dict(recent_window=1040), 1),
+    (dict(rope_theta=-1.0), 1), (dict(rope_theta=0.5), 1), (dict(rope_theta=float("inf")), 1),
+    (dict(rope_theta=float("nan")), 1), (dict(rope_theta=10000.0, max_tokens=(1 << 24) + 1), 2),
 ])
 def test_config_validation(L, kw, status):
     with pytest.raises(kvq.KVQError) as e:
