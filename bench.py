@@ -198,7 +198,8 @@ def run_ours(args, rank, world, name):
     steps, warm = args.steps, args.warmup
     e2e_steps = min(steps, max(3, steps // 2))
     cap = wl.max_tokens + warm + steps + e2e_steps + 2
-    cfg = kvq.make_config(L, B, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v, recent_window=args.window)
+    cfg = kvq.make_config(L, B, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v, recent_window=args.window,
+                          rope_theta=args.rope)
     cache = kvq.KVQCache(cfg, device=dev)
     cache.kvq_set_decode_plan(cap)
     # prefill every layer from GPU-generated synthetic data (layer by layer)
@@ -360,7 +361,8 @@ def run_ours(args, rank, world, name):
             "vs_baseline": None, "dtype": "fp16 in, 2..8-bit codes, fp32 accumulate", "data": "synthetic",
             "pct_of_peak": round(100.0 * value / peak, 2),
             "cached_tokens_per_s": round(tokens_all / (t_max * 1e-3), 1),
-            "config": {"workload": wl.name + (f"_w{args.window}" if args.window else ""), "layers": L,
+            "config": {"workload": wl.name + (f"_w{args.window}" if args.window else "") +
+                       (f"_rope{args.rope:g}" if args.rope else ""), "layers": L, "rope_theta": args.rope,
                        "batch_per_gpu": B, "q_heads": Hq, "kv_heads": H, "recent_window": args.window,
                        "head_dim": D, "cached_tokens": wl.lens[0], "k": list(wl.k), "v": list(wl.v),
                        "k_format": "bits,group,axis(0 per-token,1 per-channel),mode(0 asym,1 sym)",
@@ -586,6 +588,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=0, help="cap the cached tokens per sequence (profiling runs)")
     ap.add_argument("--window", type=int, default=0,
                     help="full-precision recent window of both tensors (multiple of 16; 0 = none)")
+    ap.add_argument("--rope", type=float, default=0.0,
+                    help="pre-RoPE key cache: rotary base applied to the dequantized keys at decode (0 = none)")
     ap.add_argument("--materialized", action="store_true",
                     help="also time the materialised baseline (dequantize to fp16, then decode) beside the fused path")
     args = ap.parse_args()
