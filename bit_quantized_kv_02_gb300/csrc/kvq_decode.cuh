@@ -194,32 +194,47 @@ __device__ __forceinline__ void load_meta2(const char* meta, int c, int meta_f32
 // each 16-channel chunk further by chi (the conversion's column scale), and
 // split into fp16 hi + lo; bias[rho] = sum_c q_c zero'_c with zero' = zero -
 // conv_off * step (symmetric zero = -2^(B-1) step).  Only valid query columns
-// are written; the rest of barea stays zero.
+// are written; the rest of barea stays zero.  Each lane loads the metadata of
+// its channels once for every query, and the per-query bias partials are
+// summed by one reduce-scatter butterfly over the warp.
 template <int D, bool R8>
 __device__ __forceinline__ void build_qb(const float* qs, int rep, const char* kmeta, int kbits, int ksym, int kf32,
                                          uint32_t* barea, float* bias, int E, float chi, int lane) {
+  constexpr int IT = D / 64;  // channel pairs per lane
   const float sc = exp2i(E);
   const float koff = (float)conv_off(kbits), ksoff = (float)(1 << (kbits - 1));
-  for (int rho = 0; rho < rep; ++rho) {
-    float bacc = 0.0f;
+  float sm0[IT], sm1[IT], zq0[IT], zq1[IT];  // per channel: operand scale, folded zero point
 #pragma unroll
-    for (int it = 0; it < D / 64; ++it) {
+  for (int it = 0; it < IT; ++it) {
+    const int c = 2 * (lane + 32 * it);
+    const float scc = (c & 8) ? sc * chi : sc;
+    sm0[it] = scc;
+    sm1[it] = scc;
+    zq0[it] = zq1[it] = 0.0f;
+    if (kmeta) {
+      float z0, st0, z1, st1;
+      load_meta2(kmeta, c, kf32, ksym, &z0, &st0, &z1, &st1);
+      if (ksym) {
+        z0 = -st0 * ksoff;
+        z1 = -st1 * ksoff;
+      }
+      sm0[it] = st0 * scc;
+      sm1[it] = st1 * scc;
+      zq0[it] = z0 - koff * st0;
+      zq1[it] = z1 - koff * st1;
+    }
+  }
+  float bpart[8];  // this lane's bias partial of each query
+#pragma unroll
+  for (int rho = 0; rho < 8; ++rho) {
+    bpart[rho] = 0.0f;
+    if (rho >= rep) continue;
+#pragma unroll
+    for (int it = 0; it < IT; ++it) {
       const int c = 2 * (lane + 32 * it);
       const float2 q2 = *reinterpret_cast<const float2*>(qs + rho * D + c);
-      const float scc = (c & 8) ? sc * chi : sc;
-      float s0 = scc, s1 = scc;
-      if (kmeta) {
-        float z0, st0, z1, st1;
-        load_meta2(kmeta, c, kf32, ksym, &z0, &st0, &z1, &st1);
-        if (ksym) {
-          z0 = -st0 * ksoff;
-          z1 = -st1 * ksoff;
-        }
-        s0 = st0 * scc;
-        s1 = st1 * scc;
-        bacc += q2.x * (z0 - koff * st0) + q2.y * (z1 - koff * st1);
-      }
-      const float v0 = q2.x * s0, v1 = q2.y * s1;
+      if (kmeta) bpart[rho] += q2.x * zq0[it] + q2.y * zq1[it];
+      const float v0 = q2.x * sm0[it], v1 = q2.y * sm1[it];
       const __half2 hh = __floats2half2_rn(v0, v1);
       const float2 hf = __half22float2(hh);
       const __half2 ll = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
@@ -232,11 +247,30 @@ __device__ __forceinline__ void build_qb(const float* qs, int rep, const char* k
         barea[((2 * j + 1) * 32 + 4 * rho + ttig) * 2 + breg] = *reinterpret_cast<const uint32_t*>(&ll);
       }
     }
-    if (kmeta) {
+  }
+  if (kmeta) {
+    // reduce-scatter: after the rounds over lane bits 4, 3, 2 each lane keeps
+    // one query's partial (query index from those bits), then the last two
+    // rounds finish the sum; lanes with bits 0..1 clear write it
+    int nq = 8;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) bacc += __shfl_xor_sync(0xffffffffu, bacc, o);
-      if (lane == 0) bias[rho] = bacc;
+    for (int o = 16; o >= 4; o >>= 1) {
+      nq >>= 1;
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (k < nq) {
+          const float keep = up ? bpart[k + nq] : bpart[k];
+          const float give = up ? bpart[k] : bpart[k + nq];
+          bpart[k] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+        }
+      }
     }
+    float b = bpart[0];
+    b += __shfl_xor_sync(0xffffffffu, b, 2);
+    b += __shfl_xor_sync(0xffffffffu, b, 1);
+    const int rho = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+    if ((lane & 3) == 0 && rho < rep) bias[rho] = b;
   }
   __syncwarp();
 }
@@ -629,11 +663,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   for (int j = 0; j < NCH; ++j)
 #pragma unroll
     for (int r = 0; r < 4; ++r) O[j][r] = 0.0f;
-  float Zs[VAXIS == 0 ? GV_MAX : 1][SL::N];
+  // Per-token values: zero-point sums sum_t p_t * zero'_{t,g} of this lane's
+  // B tokens (2tig, 2tig+1, 2tig+8, 2tig+9) for the query of its B column,
+  // one per value group (groups-in-columns: one, for the lane's own group)
+  float Zs[VAXIS == 0 ? GV_MAX : 1];
 #pragma unroll
-  for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
-#pragma unroll
-    for (int s = 0; s < SL::N; ++s) Zs[jg][s] = 0.0f;
+  for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg) Zs[jg] = 0.0f;
   float Og[VAXIS == 1 ? NCH : 1][4];
   float Pg[SL::N];
 #pragma unroll
@@ -715,13 +750,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int lg_cpgk = 31 - __clz(cpgk), lg_cpgv = 31 - __clz(cpgv);
   const float2* ck_row0 = canK + g * gs_k;
   const float2* ck_row1 = canK + (g + 8) * gs_k;
-  const float2* cv_row0 = canV + g * gs_v;  // score-owner rows (zero-point sums)
-  const float2* cv_row1 = canV + (g + 8) * gs_v;
-  const int tk0 = 2 * tig;
-  const float2* cv_t0 = canV + tk0 * gs_v;  // B-operand tokens 2tig, 2tig+1, 2tig+8, 2tig+9
-  const float2* cv_t1 = canV + (tk0 + 1) * gs_v;
-  const float2* cv_t2 = canV + (tk0 + 8) * gs_v;
-  const float2* cv_t3 = canV + (tk0 + 9) * gs_v;
+  const int tk0 = 2 * tig;  // B-operand tokens 2tig, 2tig+1, 2tig+8, 2tig+9
   // Per-token values with few groups per row (2 * rep * groups <= 8): every
   // (query, value group, hi/lo) gets its own B column, so one B operand per
   // tile carries all groups' step-scaled probabilities and each m-tile (one
@@ -736,46 +765,52 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   // first fp16 row of the window, O is turned into plain units (as the
   // epilogue would) so that fp16 rows accumulate directly.
   bool o_real = false;
-  auto to_real = [&]() {
+  // Lane holding, after the reduction over tig, the zero-point sums of
+  // (query rho, value group jg): the lanes whose B column is that query's hi
+  // column (groups-in-columns: of that group).
+  auto zsrc = [&](int rho, int jg) { return 4 * (R8 ? rho : (GC ? 2 * (rho * gs_v + jg) : 2 * rho)); };
+  // Add the zero-point sums to O (in plain units), for every output element
+  // of this lane: (channel c, query rho0 / rho1).  The group of a channel is
+  // the same across the warp for each (j, rr).
+  auto add_zero_terms = [&]() {
+    float tz[VAXIS == 0 ? GV_MAX : 1];
 #pragma unroll
-    for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
-#pragma unroll
-      for (int q = 0; q < SL::N; ++q) {
-        float v = Zs[jg][q];
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        Zs[jg][q] = v;
-      }
+    for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u) {
+      float v = Zs[u];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      tz[u] = v;
+    }
     const int lg_gsz = vwhole ? 30 : v_lgG;
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const int c = 16 * j + g + 8 * rr, jg = c >> lg_gsz;
-        float z0 = 0.f, z1 = 0.f;
+        const int jg = (16 * j + 8 * rr) >> lg_gsz;
+        float zsel = 0.0f;
+        if (GC) zsel = tz[0];
+        else {
 #pragma unroll
-        for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u) {
-          const float zt = __shfl_sync(0xffffffffu, Zs[u][0] + Zs[u][1], min(tig / max(gs_v, 1), rep - 1));
-          if (u == jg) {
-            if (R8) {
-              z0 = Zs[u][0] + Zs[u][2];
-              z1 = Zs[u][1] + Zs[u][3];
-            } else if (GC) {
-              z0 = (tig % gs_v == jg) ? zt : 0.0f;
-            } else {
-              z0 = Zs[u][0] + Zs[u][1];
-            }
-          }
+          for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u)
+            if (u == jg) zsel = tz[u];
         }
-        const float osc = inv_sc_v * exp2i(-v_cg - (rr ? v_cr : 0));
+        const int r0 = R8 ? 2 * tig : (GC ? min(tig / gs_v, rep - 1) : min(tig, rep - 1));
+        const float z0 = __shfl_sync(0xffffffffu, zsel, zsrc(r0, jg));
+        const float z1 = R8 ? __shfl_sync(0xffffffffu, zsel, zsrc(2 * tig + 1, jg)) : 0.0f;
+        const float osc = inv_sc_v * exp2i(-v_cg - (rr ? v_cr : 0));  // 2^-E_v and the row exponent
         O[j][2 * rr] = O[j][2 * rr] * osc + z0;
         O[j][2 * rr + 1] = O[j][2 * rr + 1] * osc + z1;
       }
     }
+  };
+  // Per-token values: the packed tiles accumulate O in scaled units (2^E_v, the
+  // conversion's row exponent) with the zero points apart in Zs; before the
+  // first fp16 row of the window, O is turned into plain units (as the
+  // epilogue would) so that fp16 rows accumulate directly.
+  auto to_real = [&]() {
+    add_zero_terms();
 #pragma unroll
-    for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
-#pragma unroll
-      for (int q = 0; q < SL::N; ++q) Zs[jg][q] = 0.0f;
+    for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg) Zs[jg] = 0.0f;
     o_real = true;
   };
 
@@ -845,10 +880,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       load_b();
     }
     if (vp) {
-      if (VAXIS == 0)
-        canon_meta(reinterpret_cast<const char*>(st + st_vm), kTile * gs_v, vbits, vsym, vf32, sc_v, sc_v * v_chi,
-                   8 * gs_v, canV, lane, vcen);
-      else if (vflush)
+      if (VAXIS == 1 && vflush)
         canon_meta(reinterpret_cast<const char*>(st + st_vm), D, vbits, vsym, vf32, exp2i(-v_cg), exp2i(-v_cg - v_cr), 0,
                    canV, lane);
     }
@@ -1094,10 +1126,19 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           }
         }
 #pragma unroll
-        for (int q = 0; q < SL::N; ++q) {
-          Pg[q] *= alpha[q];
+        for (int q = 0; q < SL::N; ++q) Pg[q] *= alpha[q];
+        if (VAXIS == 0) {
+          // the zero-point sums follow the query of this lane's B column
+          float az;
+          if (!R8) {
+            az = __shfl_sync(0xffffffffu, alpha[0], min(pv_rho, rep - 1));
+          } else {
+            const float ae = __shfl_sync(0xffffffffu, alpha[0], g >> 1);
+            const float ao = __shfl_sync(0xffffffffu, alpha[1], g >> 1);
+            az = (g & 1) ? ao : ae;
+          }
 #pragma unroll
-          for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg) Zs[jg][q] *= alpha[q];
+          for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg) Zs[jg] *= az;
         }
       }
     }
@@ -1131,15 +1172,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         }
       }
       const uint32_t* vtile = reinterpret_cast<const uint32_t*>(st + st_vc);
-      if (VAXIS == 0 && vp) {
-#pragma unroll
-        for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg) {
-          if (jg < gs_v) {
-#pragma unroll
-            for (int q = 0; q < SL::N; ++q) Zs[jg][q] += p[q] * (SL::rh(q) ? cv_row1 : cv_row0)[jg].y;
-          }
-        }
-      }
       if (VAXIS == 1) {
 #pragma unroll
         for (int q = 0; q < SL::N; ++q) Pg[q] += p[q];
@@ -1172,15 +1204,35 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           }
         }
       };
+      // Per-token values: the stored (zero, step) of this lane's B tokens, read
+      // straight from the stage; the B operand is p * step (with the value
+      // normalisation and, for tokens 8..15, the conversion's column scale) and
+      // the zero-point sums take p * zero' (zero' = zero - conv_off * step, or
+      // zero + 2^(B-1) * step when the codes are centred).
+      const char* vraw = reinterpret_cast<const char*>(st + st_vm);
+      const float voff = (float)conv_off(vbits), vsoff = (float)(1 << (vbits - 1));
+      auto vgroup = [&](int jg, float* zacc) {
+        float sv[4], zv[4];
+        const int tk[4] = {tk0, tk0 + 1, tk0 + 8, tk0 + 9};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float z, st;
+          load_meta(vraw, tk[k] * gs_v + jg, vf32, vsym, &z, &st);
+          sv[k] = st;
+          zv[k] = vcen ? (vsym ? 0.0f : fmaf(vsoff, st, z)) : ((vsym ? -st * vsoff : z) - voff * st);
+        }
+        const float s_lo = sc_v, s_hi = sc_v * v_chi;
+        make_b(pv[0] * s_lo * sv[0], pv[1] * s_lo * sv[1], pv[2] * s_hi * sv[2], pv[3] * s_hi * sv[3]);
+        *zacc += pv[0] * zv[0] + pv[1] * zv[1] + pv[2] * zv[2] + pv[3] * zv[3];
+      };
       auto pv_packed = [&](auto vb) {
         constexpr int VB = decltype(vb)::value;
-        if (GC)
-          make_b(pv[0] * cv_t0[gc_grp].x, pv[1] * cv_t1[gc_grp].x, pv[2] * cv_t2[gc_grp].x, pv[3] * cv_t3[gc_grp].x);
+        if (GC) vgroup(gc_grp, &Zs[0]);
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           if (VAXIS == 0 && !GC && (j & (cpgv - 1)) == 0) {
             const int jg = j >> lg_cpgv;
-            make_b(pv[0] * cv_t0[jg].x, pv[1] * cv_t1[jg].x, pv[2] * cv_t2[jg].x, pv[3] * cv_t3[jg].x);
+            vgroup(jg, &Zs[VAXIS == 0 ? jg : 0]);
           }
           uint32_t A[4];
           convert_chunk<VB, D>(vtile, lane, j, A);
@@ -1299,31 +1351,13 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     mq0 = m_run[0];
     mq1 = m_run[1];
   }
-  if (VAXIS == 0) {
-#pragma unroll
-    for (int jg = 0; jg < (VAXIS == 0 ? GV_MAX : 1); ++jg)
-#pragma unroll
-      for (int q = 0; q < SL::N; ++q) {
-        float v = Zs[jg][q];
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        Zs[jg][q] = v;
-      }
-  }
+  // per-token values still in scaled units: O becomes plain units plus the zero terms
+  if (VAXIS == 0 && !o_real) to_real();
   __syncthreads();  // stages are free: reuse them for the CTA merge
   float* mw = reinterpret_cast<float*>(smem + CFG::head_bytes(a));  // [4][rep][D+2]
   const int rowlen = D + 2;
   {
     const int lg_gsz = (VAXIS == 0 && !vwhole) ? v_lgG : 30;  // channel group of an output column
-    // groups-in-columns: this lane's columns belong to query tig / groups and
-    // value group tig % groups; the zero-point sums of that query come from
-    // the score-owner lanes of query rho (lane rho holds them after the reduction)
-    float zq[VAXIS == 0 ? GV_MAX : 1];
-    if (VAXIS == 0 && GC) {
-#pragma unroll
-      for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u)
-        zq[u] = __shfl_sync(0xffffffffu, Zs[u][0] + Zs[u][1], min(tig / gs_v, rep - 1));
-    }
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
 #pragma unroll
@@ -1342,19 +1376,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           v1 = O[j][2 * rr + 1];
           rho0 = 2 * tig;
           rho1 = 2 * tig + 1;
-        }
-        if (VAXIS == 0 && !o_real) {
-          const int jg = c >> lg_gsz;
-          float z0 = 0.f, z1 = 0.f;
-#pragma unroll
-          for (int u = 0; u < (VAXIS == 0 ? GV_MAX : 1); ++u)
-            if (u == jg) {
-              z0 = R8 ? (Zs[u][0] + Zs[u][2]) : (GC ? zq[u] : (Zs[u][0] + Zs[u][1]));
-              z1 = R8 ? (Zs[u][1] + Zs[u][3]) : 0.0f;
-            }
-          const float osc = inv_sc_v * exp2i(-v_cg - (rr ? v_cr : 0));  // 2^-E_v and the conversion's row exponent
-          v0 = v0 * osc + z0;
-          v1 = v1 * osc + z1;
         }
         if (rho0 >= 0 && rho0 < rep) mw[(warp * rep + rho0) * rowlen + c] = v0;
         if (rho1 >= 0 && rho1 < rep) mw[(warp * rep + rho1) * rowlen + c] = v1;

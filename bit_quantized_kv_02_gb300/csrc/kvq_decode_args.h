@@ -132,7 +132,7 @@ __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, in
   L.barea_bytes = (D / 16) * 32 * 8 * (rep == 8 ? 2 : 1);
   // per-channel keys are read from the stage, except by the rotary kernel, which keeps the group's D entries
   L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : (rope ? D : 0);
-  L.canon_v = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) : D;
+  L.canon_v = vaxis == 0 ? 0 : D;  // per-token values are read from the stage
   L.stage_off = dl_round(L.barea_bytes + (L.canon_k + L.canon_v) * 8 + 32, 128);
   L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns), 128);
   const int merge_bytes = 4 * rep * (D + 2) * 4;
