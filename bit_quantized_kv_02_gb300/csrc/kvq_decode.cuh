@@ -280,11 +280,7 @@ struct IntC {
   static constexpr int value = V;
 };
 
-// stage index of tile i: a constant inside an unrolled block, or i mod stages
-template <int S>
-struct StageC {
-  __device__ static constexpr int get(int) { return S; }
-};
+// stage index of tile i: i mod stages
 struct StageR {
   int mask;
   __device__ int get(int i) const { return i & mask; }
@@ -534,7 +530,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const char* km_g = km_src + lane * 16;
   const char* vm_g = vm_src + lane * 16;
   auto lane_copy = [&](uint32_t sdst, const char* gsrc, int bytes) {
-    for (int o = 0; o < bytes - lane * 16; o += 512) cp_async16_s(sdst + o, gsrc + o);
+#pragma unroll 4
+    for (int o = 0; o < bytes; o += 512)  // uniform trip count; a lane's last piece is predicated
+      if (o + lane * 16 < bytes) cp_async16_s(sdst + o, gsrc + o);
   };
   const int f16st = CFG::stage_f16(a);
   auto issue = [&](int i) {
@@ -748,8 +746,6 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int cpgk = k_token ? (kwhole ? NCH : (kG >> 4)) : NCH;  // chunks per key group (per-token keys)
   const int cpgv = VAXIS == 0 ? (vwhole ? NCH : (vG >> 4)) : NCH;
   const int lg_cpgk = 31 - __clz(cpgk), lg_cpgv = 31 - __clz(cpgv);
-  const float2* ck_row0 = canK + g * gs_k;
-  const float2* ck_row1 = canK + (g + 8) * gs_k;
   const int tk0 = 2 * tig;  // B-operand tokens 2tig, 2tig+1, 2tig+8, 2tig+9
   // Per-token values with few groups per row (2 * rep * groups <= 8): every
   // (query, value group, hi/lo) gets its own B column, so one B operand per
@@ -863,8 +859,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           qb_state = 0;
           load_b();
         }
-        canon_meta(reinterpret_cast<const char*>(st + st_km), kTile * gs_k, kbits, ksym, kf32, exp2i(-Ek - k_cg),
-                   exp2i(-Ek - k_cg - k_cr), 8 * gs_k, canK, lane);
+        // (per-token key metadata is read raw from the stage by the fold below)
       } else if ((t0 & kgmask) == 0) {
         Ek = E_chan;
         build_qb<D, R8>(qs, rep, reinterpret_cast<const char*>(st + st_km), kbits, ksym, kf32, barea, wbias, E_chan,
@@ -897,16 +892,31 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       const bool ktok = kp && k_token;
       // packed keys: undo 2^Ek and the conversion's row exponent
       const float inv_e0 = exp2i(-Ek - (kp ? k_cg : 0)), inv_e1 = exp2i(-Ek - (kp ? k_cg + k_cr : 0));
+      // per-token keys: the stored (zero, step) of this lane's two score rows
+      // for group jg, straight from the stage; the step takes the query and
+      // conversion scales of its row half, the zero point (zero - conv_off *
+      // step; symmetric -2^(B-1) step) multiplies the group's query sum
+      const char* kraw = reinterpret_cast<const char*>(st + st_km);
+      const float kpost0 = exp2i(-Ek - k_cg), kpost1 = exp2i(-Ek - k_cg - k_cr);
+      const float koff = (float)conv_off(kbits), ksoff = (float)(1 << (kbits - 1));
       auto fold = [&](int jg) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) C[r] += C2[r];
+        float ks0 = 0.f, kz0 = 0.f, ks1 = 0.f, kz1 = 0.f;
+        if (ktok) {
+          load_meta(kraw, g * gs_k + jg, kf32, ksym, &kz0, &ks0);
+          load_meta(kraw, (g + 8) * gs_k + jg, kf32, ksym, &kz1, &ks1);
+          kz0 = (ksym ? -ks0 * ksoff : kz0) - koff * ks0;
+          kz1 = (ksym ? -ks1 * ksoff : kz1) - koff * ks1;
+          ks0 *= kpost0;
+          ks1 *= kpost1;
+        }
 #pragma unroll
         for (int q = 0; q < SL::N; ++q) {
           const float v = R8 ? C[q] : (C[2 * q] + C[2 * q + 1]);
           if (ktok) {
-            const float2 m = (SL::rh(q) ? ck_row1 : ck_row0)[jg];
             const int rho = min(SL::rho(q, tig), rep - 1);
-            score[q] += m.x * v + m.y * qg[jg * rep + rho];
+            score[q] += (SL::rh(q) ? ks1 : ks0) * v + (SL::rh(q) ? kz1 : kz0) * qg[jg * rep + rho];
           } else if (kp) {
             score[q] += v * (SL::rh(q) ? inv_e1 : inv_e0) + wbias[SL::rho(q, tig)];
           } else {
@@ -1304,25 +1314,13 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   };
 
   {
-    // fully packed, full tiles first (unrolled by the stage count when it is a
-    // compile-time constant), then the tail / partial tiles
+    // fully packed, full tiles first, then the tail / partial tiles.  One tile
+    // body per loop (no unrolling by the stage count): measured on GB300, the
+    // four-body loop overflowed the instruction cache (the top stall was "no
+    // instruction") and ran 20-27 % slower on every benchmarked workload.
     const int lim = min(min(sealed_k, sealed_v), w1);
     const int nfast = lim > w0 ? (lim - w0) >> 4 : 0;
     int i = 0;
-    constexpr int NSC = CFG::kStaticStages;
-    if constexpr (NSC == 4) {
-      for (; i + 4 <= nfast; i += 4) {
-        tile_body(i, StageC<0>{}, IntC<1>{});
-        tile_body(i + 1, StageC<1>{}, IntC<1>{});
-        tile_body(i + 2, StageC<2>{}, IntC<1>{});
-        tile_body(i + 3, StageC<3>{}, IntC<1>{});
-      }
-    } else if constexpr (NSC == 2) {
-      for (; i + 2 <= nfast; i += 2) {
-        tile_body(i, StageC<0>{}, IntC<1>{});
-        tile_body(i + 1, StageC<1>{}, IntC<1>{});
-      }
-    }
     for (; i < nfast; ++i) tile_body(i, StageR{ns - 1}, IntC<1>{});
     for (; i < ntl; ++i) tile_body(i, StageR{ns - 1}, IntC<0>{});
   }
