@@ -223,6 +223,27 @@ __device__ __forceinline__ int quant_code_r(float x, float z, float s, float r, 
   return (int)t + (1 << (bits - 1));
 }
 
+// The same code again, cheaper per element (the prefill kernels): r is the
+// step's reciprocal or 0 for a zero step.  q0 = (x - z) * r is rounded to the
+// nearest integer, ties to even, by adding and removing 1.5 * 2^23 (exact for
+// |q0| < 2^22), and the distance to that integer comes from the same sums; a
+// quotient within 2^-12 of a half-integer, beyond 512, or a subnormal
+// reciprocal takes the IEEE division, exactly as in quant_code_r.
+__device__ __forceinline__ int quant_code_fast(float x, float z, float s, float r, int bits, int sym) {
+  const float num = sym ? x : __fsub_rn(x, z);
+  const float q0 = __fmul_rn(num, r);
+  const float c = __fsub_rn(__fadd_rn(q0, 12582912.0f), 12582912.0f);
+  const float e = __fsub_rn(q0, c);
+  float t = c;
+  if (!(fabsf(q0) <= 512.0f && fabsf(e) < 0.499755859375f && (r >= 0x1p-125f || s == 0.0f)))
+    t = rintf(__fdiv_rn(num, s));
+  if (s == 0.0f) t = 0.0f;
+  int q = (int)t;
+  if (!sym) return min(max(q, 0), (1 << bits) - 1);
+  const int qmax = (1 << (bits - 1)) - 1;
+  return min(max(q, -qmax), qmax) + (1 << (bits - 1));
+}
+
 __device__ __forceinline__ int quant_code(float x, float z, float s, int bits, int sym) {
   if (s == 0.0f) return sym ? (1 << (bits - 1)) : 0;
   if (!sym) {

@@ -248,7 +248,12 @@ __device__ __forceinline__ void build_qb(const float* qs, int rep, const char* k
       }
     }
   }
-  if (kmeta) {
+  if (kmeta && rep == 1) {
+    float b = bpart[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
+    if (lane == 0) bias[0] = b;
+  } else if (kmeta) {
     // reduce-scatter: after the rounds over lane bits 4, 3, 2 each lane keeps
     // one query's partial (query index from those bits), then the last two
     // rounds finish the sum; lanes with bits 0..1 clear write it
@@ -879,7 +884,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         canon_meta(reinterpret_cast<const char*>(st + st_vm), D, vbits, vsym, vf32, exp2i(-v_cg), exp2i(-v_cg - v_cr), 0,
                    canV, lane);
     }
-    __syncwarp();
+    // the entries written above are read by other lanes below (build_qb and
+    // load_b synchronise on their own): a warp barrier only where this tile wrote any
+    if (ROPE || (VAXIS == 1 && vflush)) __syncwarp();
 
     // ------------------------------------------------------------ QK ----
     float score[SL::N];

@@ -20,7 +20,7 @@
 //      owns up to 32 channels of one row and lanes sharing a group finish the
 //      reduction with shuffles.  min / max / absmax are exact in any order;
 //   3. each element's code (the step's reciprocal with the IEEE-division
-//      fallback near half-integers, quant_code_r) is written back over its
+//      fallback near half-integers, quant_code_fast) is written back over its
 //      fp16 input as a 16-bit integer;
 //   4. ldmatrix (.trans for values) delivers every lane the codes of exactly
 //      its own fragment positions of each 16-token tile (kvq_common.cuh), so
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_channel_fast(Quant
     const float lo = (i & 1) ? __high2float(mn[i / 2]) : __low2float(mn[i / 2]);
     const float hi = (i & 1) ? __high2float(mx[i / 2]) : __low2float(mx[i / 2]);
     group_params(lo, hi, fmaxf(fabsf(lo), fabsf(hi)), a.L.bits, a.L.sym, a.L.meta_f32, &z[i], &s[i]);
-    rc[i] = __frcp_rn(s[i]);
+    rc[i] = s[i] > 0.0f ? __frcp_rn(s[i]) : 0.0f;
     store_meta(meta, mrow + i, a.L.meta_f32, a.L.sym, z[i], s[i]);
     smax_local = fmaxf(smax_local, s[i]);
   }
@@ -213,8 +213,8 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_channel_fast(Quant
 #pragma unroll
     for (int i = 0; i < CPL / 2; ++i) {
       const float2 v = __half22float2(*reinterpret_cast<const __half2*>(row + i));
-      const uint32_t c0 = (uint32_t)quant_code_r(v.x, z[2 * i], s[2 * i], rc[2 * i], a.L.bits, a.L.sym);
-      const uint32_t c1 = (uint32_t)quant_code_r(v.y, z[2 * i + 1], s[2 * i + 1], rc[2 * i + 1], a.L.bits, a.L.sym);
+      const uint32_t c0 = (uint32_t)quant_code_fast(v.x, z[2 * i], s[2 * i], rc[2 * i], a.L.bits, a.L.sym);
+      const uint32_t c1 = (uint32_t)quant_code_fast(v.y, z[2 * i + 1], s[2 * i + 1], rc[2 * i + 1], a.L.bits, a.L.sym);
       row[i] = c0 | (c1 << 16);
     }
   }
@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_token_fast(QuantAr
     if (t < valid) {
       float z, s;
       group_params(mn, mx, fmaxf(fabsf(mn), fabsf(mx)), a.L.bits, a.L.sym, a.L.meta_f32, &z, &s);
-      const float rc = __frcp_rn(s);
+      const float rc = s > 0.0f ? __frcp_rn(s) : 0.0f;
       const int j = part / lpg;
       if ((part & (lpg - 1)) == 0)
         store_meta(meta, (((long)b * a.H + h) * a.tcap + (long)tile * kTile + t) * gpr + j, a.L.meta_f32, a.L.sym, z,
@@ -288,8 +288,8 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_token_fast(QuantAr
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-          const uint32_t c0 = (uint32_t)quant_code_r(f.x, z, s, rc, a.L.bits, a.L.sym);
-          const uint32_t c1 = (uint32_t)quant_code_r(f.y, z, s, rc, a.L.bits, a.L.sym);
+          const uint32_t c0 = (uint32_t)quant_code_fast(f.x, z, s, rc, a.L.bits, a.L.sym);
+          const uint32_t c1 = (uint32_t)quant_code_fast(f.y, z, s, rc, a.L.bits, a.L.sym);
           w[i] = c0 | (c1 << 16);
         }
         src[k] = v;

@@ -5,7 +5,10 @@ rule with an IEEE division (quant_code, which the oracle also follows).
 numpy's float32 operations round to nearest like __frcp_rn / __fmul_rn /
 __fsub_rn / __fdiv_rn, so both rules are emulated exactly here and compared on
 random groups and on quotients placed at and around half-integers, across the
-2^-12 cutoff below which the reciprocal rule defers to the division."""
+2^-12 cutoff below which the reciprocal rule defers to the division.  The
+prefill kernels' form of the rule (quant_code_fast: rounding by adding and
+removing 1.5 * 2^23, the same cutoff read from the same sums) is emulated and
+compared the same way."""
 import numpy as np
 
 F = np.float32
@@ -36,6 +39,29 @@ def code_rcp(x, z, s, bits, sym):
         return np.clip(t, F(0), F((1 << bits) - 1)).astype(np.int64)
 
 
+def code_magic(x, z, s, bits, sym):
+    """The prefill kernels' form of the same rule (quant_code_fast): the
+    quotient through the step's reciprocal (0 for a zero step), rounded to the
+    nearest integer (ties to even) by adding and removing 1.5 * 2^23 in
+    float32, the distance to that integer from the same sums; near a
+    half-integer, for a quotient beyond 512 or a subnormal reciprocal the IEEE
+    division decides; the integer code is clamped like the division rule."""
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        M = F(12582912.0)
+        num = x if sym else (x - z).astype(F)
+        r = np.where(s > 0, (F(1) / s).astype(F), F(0)).astype(F)
+        q0 = (num * r).astype(F)
+        c = ((q0 + M).astype(F) - M).astype(F)
+        e = (q0 - c).astype(F)
+        fast = (np.abs(q0) <= F(512)) & (np.abs(e) < F(0.5 - 2.0 ** -12)) & ((r >= F(2.0 ** -125)) | (s == 0))
+        t = np.where(fast, c, np.rint(num / s)).astype(np.float64)
+        t = np.where(s == 0, 0.0, t)
+        if sym:
+            qmax = (1 << (bits - 1)) - 1
+            return (np.clip(t, -qmax, qmax) + (1 << (bits - 1))).astype(np.int64)
+        return np.clip(t, 0, (1 << bits) - 1).astype(np.int64)
+
+
 def fp16_steps(rng, n, lo=-14, hi=8):
     """Positive steps as stored in fp16 metadata (normal fp16 values)."""
     return np.ldexp(1.0 + rng.integers(0, 1024, n) / 1024.0, rng.integers(lo, hi, n)).astype(F)
@@ -51,6 +77,7 @@ def test_random_groups_agree():
         x = (z + rng.uniform(-0.1, levels + 0.1, n).astype(F) * s).astype(F)
         for sym in (False, True):
             np.testing.assert_array_equal(code_rcp(x, z, s, bits, sym), code_div(x, z, s, bits, sym))
+            np.testing.assert_array_equal(code_magic(x, z, s, bits, sym), code_div(x, z, s, bits, sym))
 
 
 def test_quotients_around_half_integers_agree():
@@ -67,8 +94,10 @@ def test_quotients_around_half_integers_agree():
         d = offsets[rng.integers(0, len(offsets), n)]
         x = (z.astype(np.float64) + (k + 0.5 + d) * s.astype(np.float64)).astype(F)
         np.testing.assert_array_equal(code_rcp(x, z, s, bits, False), code_div(x, z, s, bits, False))
+        np.testing.assert_array_equal(code_magic(x, z, s, bits, False), code_div(x, z, s, bits, False))
         xs = ((rng.integers(0, 2, n) * 2 - 1) * (k + 0.5 + d) * s.astype(np.float64)).astype(F)
         np.testing.assert_array_equal(code_rcp(xs, z, s, bits, True), code_div(xs, z, s, bits, True))
+        np.testing.assert_array_equal(code_magic(xs, z, s, bits, True), code_div(xs, z, s, bits, True))
 
 
 def test_cutoff_takes_the_division_near_ties():
@@ -77,6 +106,7 @@ def test_cutoff_takes_the_division_near_ties():
     z = np.zeros(4, dtype=F)
     x = (np.array([2.5, 3.5, 2.5 + 2.0 ** -14, 3.5 - 2.0 ** -14]) * np.float64(F(0.1))).astype(F)
     np.testing.assert_array_equal(code_rcp(x, z, s, 4, False), code_div(x, z, s, 4, False))
+    np.testing.assert_array_equal(code_magic(x, z, s, 4, False), code_div(x, z, s, 4, False))
 
 
 def test_degenerate_steps_agree():
@@ -88,5 +118,7 @@ def test_degenerate_steps_agree():
         for sym in (False, True):
             a = code_rcp(x, z, s, 4, sym)
             b = code_div(x, z, s, 4, sym)
+            c = code_magic(x, z, s, 4, sym)
             ok = ~np.isnan(x)
             np.testing.assert_array_equal(a[ok], b[ok])
+            np.testing.assert_array_equal(c[ok], b[ok])
