@@ -385,9 +385,10 @@ struct StatCfg {
 // --------------------------------------------------------------- kernel ----
 
 // resident CTAs per SM the register budget is sized for
-// (compile-time configurations need fewer registers than the generic kernel)
+// (compile-time configurations need fewer registers than the generic kernel;
+// measured: 5 at head_dim 128 beats 4, 3 at head_dim 256 loses to 2)
 __host__ __device__ constexpr int decode_min_blocks(int D, bool is_static) {
-  return is_static ? (D == 64 ? 5 : (D == 128 ? 4 : 2)) : (D == 64 ? 5 : (D == 128 ? 3 : 2));
+  return is_static ? (D == 64 ? 5 : (D == 128 ? 5 : 2)) : (D == 64 ? 5 : (D == 128 ? 3 : 2));
 }
 
 // FUSED: the launch also appends the new token (kvq_append_decode_attn); the
@@ -400,7 +401,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NCH = D / 16;                // 16-channel chunks / m-tiles
   constexpr int NB = R8 ? 2 : 1;             // B operands per chunk (hi/lo split over two MMAs)
-  constexpr bool BREG = NCH * 2 * NB <= 16;  // query operand kept in registers
+  // query operand kept in registers at head_dim 64; wider heads read it from
+  // shared memory per MMA (measured at head_dim 128: the 16 registers are worth
+  // more as a fifth resident CTA per SM, 6-7 % faster)
+  constexpr bool BREG = NCH * 2 * NB <= 8;
   constexpr int GV_MAX = D / 32;             // per-token value groups per head row (group >= 32)
   using SL = Slots<R8>;
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
