@@ -424,7 +424,9 @@ kvq_status kvq_set_decode_kernel(kvq_cache_t C, int which) {
 }
 
 int kvq_decode_kernel_specialized(kvq_cache_t C) {
-  return (C && C->dec_fn && C->dec_fn == decode_kernel_fast(C) && !C->generic_decode) ? 1 : 0;
+  if (!C || !C->dec_fn || C->generic_decode) return 0;
+  void* fast = C->cfg.rope_theta > 0.0f ? decode_kernel_rope_fast(C) : decode_kernel_fast(C);
+  return C->dec_fn == fast ? 1 : 0;
 }
 
 kvq_status kvq_refresh_lens(kvq_cache_t C, void* stream) {

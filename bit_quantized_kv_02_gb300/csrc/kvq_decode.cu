@@ -134,7 +134,7 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
 cudaError_t decode_setup(kvq_cache* C) {
   // pre-RoPE caches run the rotary instances of the runtime-format kernel
   const bool rope = C->cfg.rope_theta > 0.0f;
-  void* fn = (C->generic_decode || rope) ? nullptr : decode_kernel_fast(C);
+  void* fn = C->generic_decode ? nullptr : (rope ? decode_kernel_rope_fast(C) : decode_kernel_fast(C));
   if (!fn && rope) fn = pick_kernel_rope(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
   if (!fn) fn = pick_kernel(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
   if (!fn) return cudaErrorInvalidValue;

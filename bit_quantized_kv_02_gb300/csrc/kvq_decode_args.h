@@ -130,9 +130,10 @@ __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, in
   L.stage_bytes = dl_round(L.st_vm + L.vm_bytes, 128);
   L.lg_ns = L.stage_bytes <= 4096 ? 2 : 1;
   L.barea_bytes = (D / 16) * 32 * 8 * (rep == 8 ? 2 : 1);
-  // keys are read from the stage, except by the rotary kernel, which keeps their (step, zero') entries
-  L.canon_k = rope ? (kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : D) : 0;  // only the rotary kernel canonicalises keys
-  L.canon_v = vaxis == 0 ? 0 : D;  // per-token values are read from the stage
+  // per-token keys keep a tile's canonical entries; per-channel keys are read
+  // from the stage, except by the rotary kernel, which keeps the group's D entries
+  L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : (rope ? D : 0);
+  L.canon_v = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) : D;
   L.stage_off = dl_round(L.barea_bytes + (L.canon_k + L.canon_v) * 8 + 32, 128);
   L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns), 128);
   const int merge_bytes = 4 * rep * (D + 2) * 4;
@@ -153,5 +154,10 @@ void* decode_kernel_ptr_rope_d256(bool r8, int vaxis);
 
 // compile-time specialisation for this cache's formats, or null (generic kernel)
 void* decode_kernel_fast(const kvq_cache* C);
+// the second part of the specialisation table (plain and fused)
+void* decode_kernel_fast_part1(const kvq_cache* C);
+void* decode_kernel_fused_part1(const kvq_cache* C);
+// compile-time specialisation of the rotary decode kernel for this cache, or null
+void* decode_kernel_rope_fast(const kvq_cache* C);
 
 }  // namespace kvq

@@ -1,9 +1,13 @@
 // kvq_decode_fast.cu — the plain compile-time specialisations of the decode
-// kernel.  Any other format runs the generic kernel.
+// kernel, part 0 of the table (part 1: kvq_decode_fast2.cu).  Any other
+// format runs the generic kernel.
 #include "kvq_decode_table.cuh"
 
 namespace kvq {
 
-void* decode_kernel_fast(const kvq_cache* C) { return lookup_specialised<false>(C); }
+void* decode_kernel_fast(const kvq_cache* C) {
+  void* fn = lookup_specialised<false, 0>(C);
+  return fn ? fn : decode_kernel_fast_part1(C);
+}
 
 }  // namespace kvq

@@ -1,10 +1,14 @@
 // kvq_decode_fused.cu — the compile-time specialisations of the decode kernel
-// with the append of the new token fused in (kvq_append_decode_attn).  Other
-// formats run the append kernel and the decode kernel back to back.
+// with the append of the new token fused in (kvq_append_decode_attn), part 0
+// of the table (part 1: kvq_decode_fused2.cu).  Other formats run the append
+// kernel and the decode kernel back to back.
 #include "kvq_decode_table.cuh"
 
 namespace kvq {
 
-void* decode_kernel_fused(const kvq_cache* C) { return lookup_specialised<true>(C); }
+void* decode_kernel_fused(const kvq_cache* C) {
+  void* fn = lookup_specialised<true, 0>(C);
+  return fn ? fn : decode_kernel_fused_part1(C);
+}
 
 }  // namespace kvq

@@ -99,6 +99,7 @@ cudaError_t quant_setup(kvq_cache* C);
 cudaError_t decode_setup(kvq_cache* C);
 void* decode_kernel_fast(const kvq_cache* C);
 void* decode_kernel_fused(const kvq_cache* C);
+void* decode_kernel_rope_fast(const kvq_cache* C);
 
 // decode: plans the split, launches the split-K kernel (which also combines)
 cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out,

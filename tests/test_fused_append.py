@@ -34,7 +34,10 @@ CASES = [
     ("mha64_k6pt_g64", 2, 2, 2, 64, (6, 64, PT, ASYM), (4, 64, PT, ASYM), [96, 33], 34, 1),
     ("mha64_k5_v7_g16", 1, 2, 2, 64, (5, 16, PC, ASYM), (7, 32, PT, ASYM), [129], 20, 2),
     ("mha128_kc_vt", 2, 3, 3, 128, (2, 32, PC, ASYM), (2, 32, PT, ASYM), [95, 200], 40, 1),
-    ("mha128_kc_vc", 2, 3, 3, 128, (2, 32, PC, ASYM), (2, 32, PC, ASYM), [95, 200], 40, 2),
+    ("mha128_kc_vc", 2, 3, 3, 128, (2, 32, PC, ASYM), (2, 32, PC, ASYM), [95, 200], 40, 1),
+    ("mha128_kt_vt", 2, 3, 3, 128, (2, 32, PT, ASYM), (2, 32, PT, ASYM), [95, 200], 40, 1),
+    ("mha128_kt_vc", 2, 3, 3, 128, (2, 32, PT, ASYM), (2, 32, PC, ASYM), [63, 190], 40, 1),
+    ("gqa8_256_sym6_pc", 1, 8, 1, 256, (6, 32, PC, SYM), (6, 32, PT, SYM), [333], 36, 1),
     ("mha128_kt_vc_g64", 2, 2, 2, 128, (2, 32, PT, ASYM), (3, 64, PC, ASYM), [60, 130], 70, 2),
     ("gqa4_128_empty", 3, 8, 2, 128, (2, 64, PC, ASYM), (2, 64, PT, ASYM), [1000, 64, 0], 66, 1),
     ("gqa8_256_pt", 1, 16, 2, 256, (4, 32, PT, ASYM), (8, 32, PT, ASYM), [700], 20, 1),

@@ -52,17 +52,24 @@ def _workload(name, B, Hq, H, D, kc, vc, seed):
                           key_outlier_scale=12.0, seed=seed)
 
 
-@pytest.mark.parametrize("combine", [0, 2], ids=["default_merge", "global_merge"])
+@pytest.mark.parametrize("which", [0, 1, 2], ids=["default", "generic", "global_merge"])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_rope_decode_parity(case, combine):
+def test_rope_decode_parity(case, which):
+    """which: kvq_set_decode_kernel bits (0: the compile-time rotary
+    specialisation where the format has one, else the runtime-format rotary
+    kernel; 1: always the runtime-format kernel; 2: merge through the global
+    workspace)."""
     name, B, Hq, H, D, kc, vc, lens, base = case
     wl = _workload(name, B, Hq, H, D, kc, vc, seed=21)
     T = max(max(lens), 1)
     cfg = kvq.make_config(1, B, Hq, H, D, T, kc, vc, rope_theta=base)
     cache = kvq.KVQCache(cfg)
-    if combine:
-        cache.kvq_set_decode_kernel(combine)
-    assert not cache.kvq_decode_kernel_specialized()
+    if which:
+        cache.kvq_set_decode_kernel(which)
+    if which & 1:
+        assert not cache.kvq_decode_kernel_specialized()
+    elif name == "mha128_kc_vt_tail":
+        assert cache.kvq_decode_kernel_specialized()  # the Llama-2-13B format has a rotary specialisation
     k, v = wl.layer_kv(0, "cpu", T=T)
     cache.kvq_prefill_quantize(0, k.cuda(), v.cuda(), lens)
     exp = cache.kvq_export(0)
