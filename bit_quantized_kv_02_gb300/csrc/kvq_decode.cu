@@ -60,6 +60,18 @@ int round_up(int x, int m) { return (x + m - 1) / m * m; }
 // bytes of one tile's (per-token) or one group's (per-channel) metadata
 int meta_tile_bytes(const TensorLayout& L) { return kTile * (L.whole ? 1 : L.gpt) * L.meta_bytes; }
 
+// Work weight of a token in fp16 rows (see plan_launch): 1 without a window.
+int window_weight(const kvq_cache* C) {
+  if (C->k.window == 0 && C->v.window == 0) return 1;
+  const int D = C->cfg.head_dim;
+  auto packed = [&](const TensorLayout& L) {
+    const double meta = L.axis == 0 ? meta_tile_bytes(L) : (double)D * L.meta_bytes * kTile / L.group;
+    return L.tile_words * 4.0 + meta;
+  };
+  const double ratio = 2.0 * kTile * D * 2.0 / (packed(C->k) + packed(C->v));
+  return std::max(1, std::min(8, (int)std::lround(ratio)));
+}
+
 }  // namespace
 
 // Shared-memory plan and per-call split of the token range.
@@ -107,6 +119,7 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   // the cache's fp16 rows (window, unsealed groups) are read straight from
   // global memory, prefetched into L2 when their tile is issued
   a.stage_f16 = 0;
+  a.fw = 1;
   a.arrive = C->d_arrive;
   const int rope = cfg.rope_theta > 0.0f;
   a.rope_l2b = rope ? std::log2((double)cfg.rope_theta) : 0.0;
@@ -232,6 +245,18 @@ static cudaError_t plan_launch(kvq_cache* C, int layer, const void* q, int q_f32
   if (C->v.axis == 1) unit = std::max(unit, C->v.group);
   std::vector<int32_t> plan(C->lens.begin() + (long)layer * cfg.batch, C->lens.begin() + (long)(layer + 1) * cfg.batch);
   for (auto& x : plan) x = std::max(x, (int32_t)std::min(C->plan_tokens, C->cfg.max_tokens));
+  // With a full-precision window, a token still in fp16 rows counts as the
+  // ratio of an fp16 tile's bytes to a packed tile's (codes and metadata of
+  // both tensors), at most 8, so that the split spreads the window's tiles
+  // over several warps.  The kernel weighs the fp16 part from the first unit
+  // below its sealed tokens, at most window + 2 units of a sequence; the plan
+  // uses that bound (the work only grows with the length, so a launch planned
+  // for a length covers every shorter one).
+  a.fw = window_weight(C);
+  if (a.fw > 1) {
+    const int span = std::max(C->k.window, C->v.window) + 2 * unit;
+    for (auto& x : plan) x += (int32_t)((a.fw - 1) * std::min((int)x, span));
+  }
   // about four resident CTAs (16 warps) per SM already keep the issue slots
   // busy; planning for more only adds per-CTA fixed work
   const int slots = C->sm_count * std::min(occ, 4);

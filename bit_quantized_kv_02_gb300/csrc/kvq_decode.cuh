@@ -452,7 +452,29 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   }
   const int n_old = FUSED ? s_n_old : 0;
   const int n = FUSED ? n_old + 1 : a.lens[b];
-  const int nchunks = (n + S - 1) / S;
+  // tokens held as codes; the newer ones are fp16 rows (unsealed per-channel
+  // groups and the full-precision window)
+  const bool k_token = CFG::ktok(a);
+  const int k_lgG = CFG::klg(a), v_lgG = CFG::vlg(a);
+  const int kold = max(n - a.K.window, 0), vold = max(n - a.V.window, 0);
+  const int sealed_k = k_token ? (a.K.window ? (kold >> 4) << 4 : n) : ((kold >> k_lgG) << k_lgG);
+  const int sealed_v = VAXIS == 0 ? (a.V.window ? (vold >> 4) << 4 : n) : ((vold >> v_lgG) << v_lgG);
+  // Work of a (sequence, head): a token from the first fp16 unit on counts
+  // a.fw times (its rows are read with direct loads, several times a packed
+  // token's bytes), so that the window's tiles spread over several warps
+  // instead of piling up in the last one.  Chunks of S and warp ranges of Sw
+  // split the work; a range's ends map back to tokens at unit boundaries (a
+  // multiple of 16 and of every per-channel group), so a group never straddles
+  // two ranges.
+  const int unit = max(kTile, max(k_token ? 1 : CFG::kG(a), VAXIS == 0 ? 1 : CFG::vG(a)));
+  const int fw = a.fw;
+  const int bnd = fw > 1 ? (min(sealed_k, sealed_v) & ~(unit - 1)) : n;
+  const int ne = bnd + fw * (n - bnd);
+  const int nchunks = (ne + S - 1) / S;
+  auto range_end = [&](int e) {  // first token past work e
+    e = min(e, ne);
+    return e <= bnd ? e : min(n, bnd + (((e - bnd + fw - 1) / fw + unit - 1) & ~(unit - 1)));
+  };
   // every CTA of (b, h) counts itself in once its length read is complete (a
   // fence orders the read before the count); the last one to arrive advances
   // the lengths, which no CTA of this launch reads afterwards
@@ -485,10 +507,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
 
   // ---- tensor formats (constants in a compile-time configuration)
   const int kbits = CFG::kbits(a), ksym = CFG::ksym(a), kf32 = CFG::kf32(a), kwhole = CFG::kwhole(a);
-  const bool k_token = CFG::ktok(a);
-  const int kgpt = CFG::kgpt(a), k_lgG = CFG::klg(a), kG = CFG::kG(a);
+  const int kgpt = CFG::kgpt(a), kG = CFG::kG(a);
   const int vbits = CFG::vbits(a), vsym = CFG::vsym(a), vf32 = CFG::vf32(a), vwhole = CFG::vwhole(a);
-  const int vgpt = CFG::vgpt(a), v_lgG = CFG::vlg(a), vG = CFG::vG(a);
+  const int vgpt = CFG::vgpt(a), vG = CFG::vG(a);
   const int kmb = CFG::kmb(a), vmb = CFG::vmb(a);
   const int kc_bytes = CFG::kc_bytes(a), vc_bytes = CFG::vc_bytes(a);
   const int km_bytes = CFG::km_bytes(a), vm_bytes = CFG::vm_bytes(a);
@@ -510,15 +531,10 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   // (fused append: the warp whose range holds token n_old appends it before
   // it stages anything; its range holds every tile and group the append
   // writes, so no other warp or CTA reads them)
-  const bool appender = FUSED && chunk == n_old / S && warp == (n_old - chunk * S) / a.Sw;
-  const int w0 = chunk * S + warp * a.Sw;
-  const int w1 = min(w0 + a.Sw, n);
+  const int w0 = range_end(chunk * S + warp * a.Sw);
+  const int w1 = range_end(chunk * S + (warp + 1) * a.Sw);
+  const bool appender = FUSED && w0 <= n_old && n_old < w1;
   const int ntl = w1 > w0 ? (w1 - w0 + kTile - 1) / kTile : 0;
-  // tokens held as codes; the newer ones are fp16 rows (unsealed per-channel
-  // groups and the full-precision window)
-  const int kold = max(n - a.K.window, 0), vold = max(n - a.V.window, 0);
-  const int sealed_k = k_token ? (a.K.window ? (kold >> 4) << 4 : n) : ((kold >> k_lgG) << k_lgG);
-  const int sealed_v = VAXIS == 0 ? (a.V.window ? (vold >> 4) << 4 : n) : ((vold >> v_lgG) << v_lgG);
   const long bh = (long)b * H + h;
   const char* kc_src = a.K.codes + (bh * ntiles + (w0 >> 4)) * (long)kc_bytes;
   const char* vc_src = a.V.codes + (bh * ntiles + (w0 >> 4)) * (long)vc_bytes;
@@ -892,10 +908,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           qb_state = 0;
           load_b();
         }
-        // every lane folds several groups of its two rows: the tile's entries
-        // are canonicalised once, (step * row scale, zero'), 16 * groups of them
-        canon_meta(reinterpret_cast<const char*>(st + st_km), kTile * gs_k, kbits, ksym, kf32, exp2i(-Ek - k_cg),
-                   exp2i(-Ek - k_cg - k_cr), 8 * gs_k, canK, lane);
+        // (per-token key metadata is read raw from the stage by the fold below:
+        // measured, a shared canonicalisation pass per tile plus its barrier
+        // cost more than the per-lane conversions, even at 8 groups a token)
       } else if ((t0 & kgmask) == 0) {
         Ek = E_chan;
         build_qb<D, R8>(qs, rep, reinterpret_cast<const char*>(st + st_km), kbits, ksym, kf32, barea, wbias, E_chan,
@@ -911,19 +926,13 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       load_b();
     }
     if (vp) {
-      // per-token values outside the groups-in-columns mode: each lane scales
-      // its P operand by several groups; the tile's entries are canonicalised
-      // once (step * value scale (* column scale for tokens 8..15), zero')
-      if (VAXIS == 0 && !GC)
-        canon_meta(reinterpret_cast<const char*>(st + st_vm), kTile * gs_v, vbits, vsym, vf32, sc_v, sc_v * v_chi,
-                   8 * gs_v, canV, lane, vcen);
       if (VAXIS == 1 && vflush)
         canon_meta(reinterpret_cast<const char*>(st + st_vm), D, vbits, vsym, vf32, exp2i(-v_cg), exp2i(-v_cg - v_cr), 0,
                    canV, lane);
     }
     // the entries written above are read by other lanes below (build_qb and
     // load_b synchronise on their own): a warp barrier only where this tile wrote any
-    if (ROPE || k_token || (VAXIS == 0 && !GC) || (VAXIS == 1 && vflush)) __syncwarp();
+    if (ROPE || (VAXIS == 1 && vflush)) __syncwarp();
 
     // ------------------------------------------------------------ QK ----
     float score[SL::N];
@@ -936,18 +945,31 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       const bool ktok = kp && k_token;
       // packed keys: undo 2^Ek and the conversion's row exponent
       const float inv_e0 = exp2i(-Ek - (kp ? k_cg : 0)), inv_e1 = exp2i(-Ek - (kp ? k_cg + k_cr : 0));
-      // per-token keys: the canonical (step * row scale, zero') of this lane's
-      // two score rows for group jg; the zero point multiplies the group's query sum
+      // per-token keys: the stored (zero, step) of this lane's two score rows
+      // for group jg, straight from the stage; the step takes the query and
+      // conversion scales of its row half, the zero point (zero - conv_off *
+      // step; symmetric -2^(B-1) step) multiplies the group's query sum
+      const char* kraw = reinterpret_cast<const char*>(st + st_km);
+      const float kpost0 = exp2i(-Ek - k_cg), kpost1 = exp2i(-Ek - k_cg - k_cr);
+      const float koff = (float)conv_off(kbits), ksoff = (float)(1 << (kbits - 1));
       auto fold = [&](int jg) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) C[r] += C2[r];
+        float ks0 = 0.f, kz0 = 0.f, ks1 = 0.f, kz1 = 0.f;
+        if (ktok) {
+          load_meta(kraw, g * gs_k + jg, kf32, ksym, &kz0, &ks0);
+          load_meta(kraw, (g + 8) * gs_k + jg, kf32, ksym, &kz1, &ks1);
+          kz0 = (ksym ? -ks0 * ksoff : kz0) - koff * ks0;
+          kz1 = (ksym ? -ks1 * ksoff : kz1) - koff * ks1;
+          ks0 *= kpost0;
+          ks1 *= kpost1;
+        }
 #pragma unroll
         for (int q = 0; q < SL::N; ++q) {
           const float v = R8 ? C[q] : (C[2 * q] + C[2 * q + 1]);
           if (ktok) {
-            const float2 m = canK[(g + 8 * SL::rh(q)) * gs_k + jg];
             const int rho = min(SL::rho(q, tig), rep - 1);
-            score[q] += m.x * v + m.y * qg[jg * rep + rho];
+            score[q] += (SL::rh(q) ? ks1 : ks0) * v + (SL::rh(q) ? kz1 : kz0) * qg[jg * rep + rho];
           } else if (kp) {
             score[q] += v * (SL::rh(q) ? inv_e1 : inv_e0) + wbias[SL::rho(q, tig)];
           } else {
@@ -1255,21 +1277,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
       auto vgroup = [&](int jg, float* zacc) {
         float sv[4], zv[4];
         const int tk[4] = {tk0, tk0 + 1, tk0 + 8, tk0 + 9};
-        if (GC) {  // raw: one group per lane
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            float z, st;
-            load_meta(vraw, tk[k] * gs_v + jg, vf32, vsym, &z, &st);
-            sv[k] = st * (k < 2 ? sc_v : sc_v * v_chi);
-            zv[k] = vcen ? (vsym ? 0.0f : fmaf(vsoff, st, z)) : ((vsym ? -st * vsoff : z) - voff * st);
-          }
-        } else {  // canonical entries of the tile
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 m = canV[tk[k] * gs_v + jg];
-            sv[k] = m.x;
-            zv[k] = m.y;
-          }
+        for (int k = 0; k < 4; ++k) {
+          float z, st;
+          load_meta(vraw, tk[k] * gs_v + jg, vf32, vsym, &z, &st);
+          sv[k] = st * (k < 2 ? sc_v : sc_v * v_chi);
+          zv[k] = vcen ? (vsym ? 0.0f : fmaf(vsoff, st, z)) : ((vsym ? -st * vsoff : z) - voff * st);
         }
         make_b(pv[0] * sv[0], pv[1] * sv[1], pv[2] * sv[2], pv[3] * sv[3]);
         *zacc += pv[0] * zv[0] + pv[1] * zv[1] + pv[2] * zv[2] + pv[3] * zv[3];

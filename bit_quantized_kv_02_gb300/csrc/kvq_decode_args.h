@@ -52,7 +52,8 @@ struct DecodeArgs {
   const void* q;
   int q_f32;
   float scale_log2;         // softmax scale * log2(e)
-  int S, Sw;                // tokens per CTA / per warp
+  int S, Sw;                // work per CTA / per warp (tokens, fp16-row tokens counted fw times)
+  int fw;                   // work of a token still in fp16 rows (1: every token counts once)
   int max_chunks;
   float* work;              // [B][H*rep][max_chunks][D+4] chunk partials
   float* gwork;             // [B][H*rep][max_groups][D+4] group partials
@@ -130,10 +131,9 @@ __host__ __device__ constexpr DecLayout dec_layout(int D, int rep, int kbits, in
   L.stage_bytes = dl_round(L.st_vm + L.vm_bytes, 128);
   L.lg_ns = L.stage_bytes <= 4096 ? 2 : 1;
   L.barea_bytes = (D / 16) * 32 * 8 * (rep == 8 ? 2 : 1);
-  // per-token keys keep a tile's canonical entries; per-channel keys are read
-  // from the stage, except by the rotary kernel, which keeps the group's D entries
-  L.canon_k = kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : (rope ? D : 0);
-  L.canon_v = vaxis == 0 ? 16 * (vwhole ? 1 : vgpt) : D;
+  // keys are read from the stage, except by the rotary kernel, which keeps their (step, zero') entries
+  L.canon_k = rope ? (kaxis == 0 ? 16 * (kwhole ? 1 : kgpt) : D) : 0;  // only the rotary kernel canonicalises keys
+  L.canon_v = vaxis == 0 ? 0 : D;  // per-token values are read from the stage
   L.stage_off = dl_round(L.barea_bytes + (L.canon_k + L.canon_v) * 8 + 32, 128);
   L.warp_bytes = dl_round(L.stage_off + (L.stage_bytes << L.lg_ns), 128);
   const int merge_bytes = 4 * rep * (D + 2) * 4;

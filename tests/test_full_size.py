@@ -76,10 +76,11 @@ def _check(name, out, k, v, q, wl, lens, tcap, scale):
     print(f"\n{name}: row {worst[0]:.2e} elementwise {worst[1]:.2e}")
 
 
-def _build(name):
+def _build(name, window=0):
     wl = synth.workload(name, layers=1)
     cap = wl.max_tokens + 8
-    cfg = kvq.make_config(1, wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v)
+    cfg = kvq.make_config(1, wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v,
+                          recent_window=window)
     cache = kvq.KVQCache(cfg)
     cache.kvq_set_decode_plan(cap)
     k, v = wl.layer_kv(0, "cuda", T=wl.max_tokens)
@@ -126,3 +127,30 @@ def test_full_size_fused_step_sampled_parity(name):
         kx[b, :n], vx[b, :n] = k[b, :n], v[b, :n]
         kx[b, n], vx[b, n] = kn[b], vn[b]
     _check(name, out.cpu().numpy(), kx, vx, q, wl, lens, cache.tcap, scale)
+
+
+@pytest.mark.parametrize("name", ["llama2_13b_kc_vt", "serving_mix", "wide_gqa_k4v8_kt"])
+def test_full_size_window_sampled_parity(name):
+    """bench.py --window 128: the newest 128 tokens of both tensors stay fp16
+    rows; the oracle quantizes the older tokens with the same window."""
+    window = 128
+    wl, cache, k, v = _build(name, window)
+    q = wl.layer_query(0, 0, "cuda")
+    scale = np.float32(1.0 / np.sqrt(wl.head_dim))
+    out = cache.kvq_decode_attn(0, q, scale=float(scale))
+    torch.cuda.synchronize()
+    assert cache.kvq_device_status() == 0
+    rep = wl.q_heads // wl.kv_heads
+    for b, h in _samples(wl.batch, wl.kv_heads):
+        n = int(wl.lens[b])
+        heads = []
+        for x, tc in ((k, wl.k), (v, wl.v)):
+            bits, group, axis, mode = tc
+            xs = x[b:b + 1, :n, h:h + 1, :].float().cpu().numpy()
+            oq = oracle.quantize_tensor(xs, np.array([n], np.int32), cache.tcap, bits, group, axis, bool(mode),
+                                        False, window)
+            heads.append(oracle.dequant_tensor(oq, [n], bits, group, axis, bool(mode), window)[0, 0])
+        qs = q[b:b + 1, h * rep:(h + 1) * rep].float().cpu().numpy()
+        ref = oracle.attention(heads[0][None, None], heads[1][None, None], qs, np.array([n], np.int32), scale)[0]
+        row, elem = errors(out.cpu().numpy()[b, h * rep:(h + 1) * rep], ref)
+        assert row <= TOL, (name, b, h, row)

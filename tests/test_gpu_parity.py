@@ -301,6 +301,10 @@ WINDOW_CASES = [
     ("w_whole", 2, 4, 4, 64, (3, WHOLE, PT, ASYM), (3, WHOLE, PT, ASYM), [65, 140], 16),
     ("w_mha128_kc_vc", 1, 3, 3, 128, (2, 32, PC, ASYM), (2, 32, PC, ASYM), [1000], 128),
     ("w_gqa2_sym", 2, 4, 2, 128, (4, 64, PC, SYM), (4, 64, PT, SYM), [500, 3], 48),
+    # Llama-2-13B's format with its 128-token window over long, ragged sequences:
+    # the split weighs the window's fp16 tiles, so they spread over several warps
+    ("w_llama_fmt_long", 3, 2, 2, 128, (2, 32, PC, ASYM), (2, 32, PT, ASYM), [4113, 1500, 130], 128),
+    ("w_wide_gqa_long", 1, 16, 2, 256, (4, 32, PT, ASYM), (8, 32, PT, ASYM), [9000], 1024),
 ]
 
 
@@ -310,6 +314,17 @@ def test_window_parity(case, generic):
     name, B, Hq, H, D, kc, vc, lens, window = case
     wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=17)
     run_case(wl, lens, generic=generic, window=window)
+
+
+@pytest.mark.parametrize("max_splits", [0, 3], ids=["planned", "three_splits"])
+@pytest.mark.parametrize("case", [c for c in WINDOW_CASES if c[0].endswith("_long")], ids=lambda c: c[0])
+def test_window_parity_global_merge(case, max_splits):
+    """The window's weighted split with the split-K partials merged through the
+    global workspace, and with the splits capped (longer warp ranges, each
+    holding more of the window)."""
+    name, B, Hq, H, D, kc, vc, lens, window = case
+    wl = W(name, B, Hq, H, D, kc, vc, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=18)
+    run_case(wl, lens, global_combine=True, max_splits=max_splits, window=window)
 
 
 @pytest.mark.parametrize("kc,vc,window", [((4, 32, PC, ASYM), (4, 32, PT, ASYM), 32),
