@@ -149,7 +149,21 @@ FAST_CASES = [
     ("fast_d256_gqa8_pt", 1, 8, 1, 256, (4, 32, PT, ASYM), (8, 32, PT, ASYM), [1000]),
     ("fast_d256_gqa8_pc", 1, 8, 1, 256, (4, 32, PC, ASYM), (8, 32, PT, ASYM), [777]),
     ("fast_d256_sym6", 1, 16, 2, 256, (6, 32, PT, SYM), (6, 32, PT, SYM), [600]),
+    ("fast_d256_sym6_pc", 1, 16, 2, 256, (6, 32, PC, SYM), (6, 32, PT, SYM), [900]),
+    ("fast_d256_gqa8_pt_ragged", 3, 16, 2, 256, (4, 32, PT, ASYM), (8, 32, PT, ASYM), [2049, 15, 0]),
 ]
+
+
+@pytest.mark.parametrize("max_splits", [0, 2], ids=["planned", "two_splits"])
+@pytest.mark.parametrize("kaxis", [PT, PC], ids=["kt", "kc"])
+def test_d256_gqa8_global_merge(kaxis, max_splits):
+    """The head_dim 256 specialisations with eight queries per kv head (keys
+    per token and per channel) over a long and a short sequence: split-K
+    partials merged through the global workspace, and with long warp ranges
+    (two splits)."""
+    wl = W("d256_pairs", 2, 16, 2, 256, (4, 32, kaxis, ASYM), (8, 32, PT, ASYM), key_outlier_frac=0.02,
+           key_outlier_scale=12.0, seed=9)
+    run_case(wl, [5000, 333], generic=False, global_combine=True, max_splits=max_splits)
 
 
 @pytest.mark.parametrize("generic", [False, True], ids=["specialized", "generic"])
