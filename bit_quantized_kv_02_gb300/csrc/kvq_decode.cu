@@ -170,14 +170,16 @@ cudaError_t decode_setup(kvq_cache* C) {
   const int rep = C->cfg.q_heads / C->cfg.kv_heads;
   C->dec_cluster_ok = !C->global_combine && cluster_fits(fn, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
   // the fused append needs a fused specialisation, layouts where each
-  // (sequence, head) owns all it writes (no window, no whole-vector groups),
-  // its scratch inside one warp's stage ring, and the plain kernel's
-  // residency and cluster merge (the launch is planned for the plain kernel)
+  // (sequence, head) owns all it writes (no whole-vector groups; with a
+  // window the block or group leaving it is sealed by the warp whose range
+  // holds it), its scratch inside one warp's stage ring, and the plain
+  // kernel's residency and cluster merge (the launch is planned for the plain kernel)
   const int ring = (1 << P.a.lg_nstages) * P.a.stage_bytes;
   C->fused_ok = 0;
   C->dec_fn_fused = (C->generic_decode || rope) ? nullptr : decode_kernel_fused(C);
-  if (C->dec_fn_fused && C->k.window == 0 && C->v.window == 0 && !C->k.whole && !C->v.whole &&
-      fused_append_scratch(C->cfg.head_dim, C->k.axis, C->v.axis) <= ring) {
+  const int window = C->k.window || C->v.window;
+  if (C->dec_fn_fused && !C->k.whole && !C->v.whole &&
+      fused_append_scratch(C->cfg.head_dim, C->k.axis, C->v.axis, window) <= ring) {
     void* ff = C->dec_fn_fused;
     int occ_f = 0;
     e = raise_smem_limit(ff, P.smem);

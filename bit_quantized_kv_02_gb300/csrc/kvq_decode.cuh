@@ -632,16 +632,33 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   // tensor: the group it seals, if it seals one) and the rest after it; the
   // append's scratch is the ring's slots from `early` on, which hold nothing
   // until then
+  // With a full-precision window the append only stores fp16 rows; the block
+  // (per-token tensor: 16 tokens) or group (per-channel tensor) that leaves
+  // the window at this step is sealed by the warp whose range holds it
+  // (ranges are multiples of 16 and of every per-channel group, so one warp
+  // holds all of it, and no other warp or CTA reads it).
+  int kseal = -1, vseal = -1;  // first token of the block / group this warp seals
+  if (FUSED) {
+    const int kw = a.K.window, vw = a.V.window;
+    const int ku = k_token ? kTile : kG, vu = VAXIS == 0 ? kTile : vG;
+    if (kw && n - kw >= ku && ((n - kw) & (ku - 1)) == 0 && w0 <= n - kw - ku && n - kw - ku < w1)
+      kseal = n - kw - ku;
+    if (vw && n - vw >= vu && ((n - vw) & (vu - 1)) == 0 && w0 <= n - vw - vu && n - vw - vu < w1)
+      vseal = n - vw - vu;
+  }
   int early = ns;
-  if (appender) {
-    const bool seal_k = !k_token && ((n_old + 1) & (kG - 1)) == 0;
-    const bool seal_v = VAXIS == 1 && ((n_old + 1) & (vG - 1)) == 0;
-    int prot = 0x7fffffff;
-    if (k_token) prot = min(prot, n_old & ~(kTile - 1));
-    else if (seal_k) prot = min(prot, n_old + 1 - kG);
-    if (VAXIS == 0) prot = min(prot, n_old & ~(kTile - 1));
-    else if (seal_v) prot = min(prot, n_old + 1 - vG);
-    const int need = (seal_k || seal_v) ? fused_append_scratch(D, 1, 1) : 0;
+  if (appender || kseal >= 0 || vseal >= 0) {
+    int prot = 0x7fffffff, need = 0;
+    if (appender && !a.K.window) {
+      if (k_token) prot = min(prot, n_old & ~(kTile - 1));
+      else if (((n_old + 1) & (kG - 1)) == 0) prot = min(prot, n_old + 1 - kG), need = fused_append_scratch(D, 1, 1);
+    }
+    if (appender && !a.V.window) {
+      if (VAXIS == 0) prot = min(prot, n_old & ~(kTile - 1));
+      else if (((n_old + 1) & (vG - 1)) == 0) prot = min(prot, n_old + 1 - vG), need = fused_append_scratch(D, 1, 1);
+    }
+    if (kseal >= 0) prot = min(prot, kseal), need = fused_append_scratch(D, 1, 1);
+    if (vseal >= 0) prot = min(prot, vseal), need = fused_append_scratch(D, 1, 1);
     early = min(min(ns, max(0, (prot - w0) / kTile)), ns - (need + stage_bytes - 1) / stage_bytes);
   }
   issue_first(0, early);
@@ -684,12 +701,15 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   for (int i = lane; i < CFG::barea_bytes(a) / 4; i += 32) barea[i] = 0u;
   if (lane < 8) wbias[lane] = 0.0f;
   __syncthreads();
-  if (FUSED && appender) {
-    // append into the cache (scratch: this warp's idle stage ring), make the
-    // writes visible to the copies that follow, then stage the first tiles;
-    // this warp's step bounds include the steps just written
-    float kst, vst;
-    fused_append<D>(a.ap, b, h, n_old, stages + early * stage_bytes, &kst, &vst);
+  if (FUSED && (appender || kseal >= 0 || vseal >= 0)) {
+    // append / seal into the cache (scratch: this warp's idle stage ring), make
+    // the writes visible to the copies that follow, then stage the first
+    // tiles; this warp's step bounds include the steps just written
+    float kst = 0.0f, vst = 0.0f;
+    unsigned char* scratch = stages + early * stage_bytes;
+    if (appender) fused_append<D>(a.ap, b, h, n_old, scratch, &kst, &vst);
+    if (kseal >= 0) kst = fmaxf(kst, seal_window_block<D>(a.ap.k, b, h, kseal, scratch));
+    if (vseal >= 0) vst = fmaxf(vst, seal_window_block<D>(a.ap.v, b, h, vseal, scratch));
     smax_k = fmaxf(smax_k, kst);
     smax_v = fmaxf(smax_v, vst);
     __threadfence_block();  // only this warp reads what it wrote

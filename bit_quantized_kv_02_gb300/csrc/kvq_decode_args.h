@@ -85,10 +85,12 @@ struct DecodeArgs {
 };
 
 // Scratch bytes one warp needs for the fused append: a per-channel seal's
-// (3*D floats of group parameters + 16 rows of D halves); per-token tensors
-// need none.
-__host__ __device__ constexpr int fused_append_scratch(int D, int k_axis, int v_axis) {
-  return (k_axis == 1 || v_axis == 1) ? 44 * D : 0;
+// (3*D floats of group parameters + 16 rows of D halves), or with a
+// full-precision window the seal of a per-token block (16 rows of D halves +
+// 3 floats per (token, group), at most 12*D bytes for groups of 16); per-token
+// tensors without a window need none.
+__host__ __device__ constexpr int fused_append_scratch(int D, int k_axis, int v_axis, int window = 0) {
+  return (k_axis == 1 || v_axis == 1 || window) ? 44 * D : 0;
 }
 
 // Host: the append arguments of a layer (kvq_quant.cu).

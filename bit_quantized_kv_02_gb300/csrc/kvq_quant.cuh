@@ -300,6 +300,67 @@ __device__ inline float seal_channel_warp(const QuantArgs& a, int b, int h, int 
   return smax_local;
 }
 
+// One warp quantizes per-token block `tile` (tokens 16*tile .. 16*tile+15) of
+// (b, h) from its fp16 rows, once all of it is older than the window: the same
+// statistics, parameters, metadata and tile words as the CTA-wide
+// quant_token_tile (min and max are exact in any order, the largest magnitude
+// is at an end of the range, and quant_code_r gives quant_code's integer).  No
+// whole-vector groups.  scratch: 16 rows of D halves + 3 * 16 * (D / G) floats
+// (token_block_scratch bytes, 16-byte aligned).  Returns the block's largest step.
+template <int CPL>
+__device__ inline float seal_token_block_warp(const QuantArgs& a, int b, int h, int tile, unsigned char* scratch) {
+  const int lane = threadIdx.x & 31;
+  constexpr int D = CPL * 32;
+  const int G = a.L.group, gpr = D / G;
+  __half* rows = reinterpret_cast<__half*>(scratch);       // [16][D]
+  float* zs = reinterpret_cast<float*>(rows + kTile * D);  // [16 * gpr] per (token, group)
+  float* ss = zs + kTile * gpr;
+  float* rs = ss + kTile * gpr;                            // step reciprocals
+  for (int i = lane; i < kTile * D / 8; i += 32) {
+    const int r = i / (D / 8), c8 = i - r * (D / 8);
+    reinterpret_cast<uint4*>(rows)[i] = reinterpret_cast<const uint4*>(tail_row(a, b, h, (long)tile * kTile + r))[c8];
+  }
+  __syncwarp();
+  char* meta = meta_ptr(a);
+  float smax_local = 0.0f;
+  for (int gi = lane; gi < kTile * gpr; gi += 32) {  // one (token, group) per lane at a time
+    const int tt = gi / gpr, j = gi - tt * gpr;
+    const __half2* src = reinterpret_cast<const __half2*>(rows + tt * D + j * G);
+    float mn = INFINITY, mx = -INFINITY;
+    for (int c = 0; c < G / 2; ++c) {
+      const float2 f = __half22float2(src[c]);
+      mn = fminf(mn, fminf(f.x, f.y));
+      mx = fmaxf(mx, fmaxf(f.x, f.y));
+    }
+    float z, st;
+    group_params(mn, mx, fmaxf(fabsf(mn), fabsf(mx)), a.L.bits, a.L.sym, a.L.meta_f32, &z, &st);
+    zs[gi] = z;
+    ss[gi] = st;
+    rs[gi] = __frcp_rn(st);
+    store_meta(meta, (((long)b * a.H + h) * a.tcap + (long)tile * kTile + tt) * gpr + j, a.L.meta_f32, a.L.sym, z,
+               st);
+    smax_local = fmaxf(smax_local, st);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) smax_local = fmaxf(smax_local, __shfl_xor_sync(0xffffffffu, smax_local, o));
+  __syncwarp();  // group parameters written
+  auto code = [&](int t, int c) {
+    const int gi = t * gpr + c / G;
+    return (uint32_t)quant_code_r(__half2float(rows[t * D + c]), zs[gi], ss[gi], rs[gi], a.L.bits, a.L.sym);
+  };
+  uint4* dst = reinterpret_cast<uint4*>(codes_ptr(a, b, h, tile));
+  for (int q = lane; q < a.L.tile_words / 4; q += 32) {
+    uint4 v;
+    v.x = build_word_f(D, a.L.planes, a.is_value, 4 * q + 0, code);
+    v.y = build_word_f(D, a.L.planes, a.is_value, 4 * q + 1, code);
+    v.z = build_word_f(D, a.L.planes, a.is_value, 4 * q + 2, code);
+    v.w = build_word_f(D, a.L.planes, a.is_value, 4 * q + 3, code);
+    dst[q] = v;
+  }
+  if (lane == 0 && smax_local > 0.0f) atomic_max_pos(a.smax + (long)b * a.H + h, smax_local);
+  return smax_local;
+}
+
 // Per-token quantization of token n of (b, h) by one warp with lane l owning
 // the CPL = D/32 channels [l*CPL, l*CPL + CPL) (values in x): every group is
 // reduced at once over its G/CPL lanes, so the work is a few dependent steps
@@ -383,11 +444,12 @@ __device__ __forceinline__ void load_lane_row(const void* x, long off, int f32, 
 // Append of token n (the old length) of (b, h) by one warp, with the same
 // effect on the cache as the append kernel: per-token rows are quantized and
 // merged into their tile, per-channel rows go to the fp16 tail and a filled
-// group is sealed.  Only layouts without a full-precision window and without
-// whole-vector groups (each (b, h) then owns everything it writes).  Both new
-// rows come straight into registers, lane l holding channels [l*D/32,
-// (l+1)*D/32), loaded together.  scratch: the seal's (44*D bytes).
-// *kstep / *vstep: the largest key / value step written (0 when none).
+// group is sealed; a tensor with a full-precision window only stores the fp16
+// row (the block or group that leaves the window is sealed by the decode warp
+// whose range holds it).  No whole-vector groups (each (b, h) then owns
+// everything it writes).  Both new rows come straight into registers, lane l
+// holding channels [l*D/32, (l+1)*D/32), loaded together.  scratch: the seal's
+// (44*D bytes).  *kstep / *vstep: the largest key / value step written (0 when none).
 template <int D>
 __device__ __forceinline__ void fused_append_body(const AppendArgs& ap, int b, int h, int n, unsigned char* scratch,
                                                   float* kstep, float* vstep) {
@@ -402,11 +464,11 @@ __device__ __forceinline__ void fused_append_body(const AppendArgs& ap, int b, i
     const QuantArgs& q = t ? ap.v : ap.k;
     const float* x = t ? xv : xk;
     float st = 0.0f;
-    if (q.L.axis == 1) {
+    if (q.L.axis == 1 || q.L.window) {
       __half2* row = reinterpret_cast<__half2*>(tail_row(q, b, h, n) + lane * CPL);
 #pragma unroll
       for (int i = 0; i < CPL; i += 2) row[i / 2] = __halves2half2(__float2half_rn(x[i]), __float2half_rn(x[i + 1]));
-      if (((n + 1) & (q.L.group - 1)) == 0) {
+      if (!q.L.window && ((n + 1) & (q.L.group - 1)) == 0) {
         __syncwarp();  // the new row is in the tail
         st = seal_channel_warp<CPL>(q, b, h, (n + 1) / q.L.group - 1, scratch);
       }
@@ -427,6 +489,19 @@ template <int D>
 static __device__ __noinline__ void fused_append_call(const AppendArgs& ap, int b, int h, int n,
                                                       unsigned char* scratch, float* kstep, float* vstep) {
   fused_append_body<D>(ap, b, h, n, scratch, kstep, vstep);
+}
+
+// Seal, inside a fused append + decode launch, the block (per-token tensor:
+// the 16 tokens from t0) or group (per-channel tensor) of (b, h) that leaves
+// the full-precision window, from its fp16 rows; returns its largest step.
+// Out of line: it runs once per 16 or G steps of a sequence.
+template <int D>
+static __device__ __noinline__ float seal_window_block(const QuantArgs& q, int b, int h, int t0,
+                                                       unsigned char* scratch) {
+  const float st = q.L.axis == 1 ? seal_channel_warp<D / 32>(q, b, h, t0 / q.L.group, scratch)
+                                 : seal_token_block_warp<D / 32>(q, b, h, t0 / kTile, scratch);
+  __syncwarp();  // scratch free for the next tensor
+  return st;
 }
 
 template <int D>

@@ -52,11 +52,11 @@ def step_tokens(wl, n0, steps):
     return wl.layer_kv(0, "cpu", T=T)
 
 
-def run_steps(wl, n0, steps, fused_kernel_bits=0, plan_tokens=0, check_every=10):
+def run_steps(wl, n0, steps, fused_kernel_bits=0, plan_tokens=0, check_every=10, window=0):
     T = max(n0) + steps
     k, v = step_tokens(wl, n0, steps)
-    a = make_cache(wl, max_tokens=T)
-    b = make_cache(wl, max_tokens=T)
+    a = make_cache(wl, max_tokens=T, window=window)
+    b = make_cache(wl, max_tokens=T, window=window)
     for c in (a, b):
         if fused_kernel_bits:
             c.kvq_set_decode_kernel(fused_kernel_bits)
@@ -100,11 +100,11 @@ def run_steps(wl, n0, steps, fused_kernel_bits=0, plan_tokens=0, check_every=10)
             pad = b.tcap - kk.shape[1]
             kk = torch.nn.functional.pad(kk, (0, 0, 0, 0, 0, pad))
             vv = torch.nn.functional.pad(vv, (0, 0, 0, 0, 0, pad))
-            ok = oracle_tensor(kk, lens, b.tcap, wl.k, False)
-            ov = oracle_tensor(vv, lens, b.tcap, wl.v, False)
+            ok = oracle_tensor(kk, lens, b.tcap, wl.k, False, window)
+            ov = oracle_tensor(vv, lens, b.tcap, wl.v, False, window)
             assert_export_equal(exp_b, ok, wl.k, "k")
             assert_export_equal(exp_b, ov, wl.v, "v")
-            ref = decode_ref(wl, ok, ov, lens, q, scale)
+            ref = decode_ref(wl, ok, ov, lens, q, scale, window)
             assert rel_err_rows(out_b.cpu().numpy(), ref).max() <= TOL, s
     return fused_launches
 
@@ -114,6 +114,34 @@ def test_fused_append_matches_separate_calls(case):
     name, B, Hq, H, D, kc, vc, n0, steps, launches = case
     wl = W(name, B, Hq, H, D, kc, vc, torch.float32, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=5)
     assert run_steps(wl, n0, steps) == {launches}
+
+
+# Full-precision recent window ("O Seu Cache KV Nao Tem um Problema de Bits...",
+# section "O Imposto dos Sistemas e Por Que Nao E um Detalhe"): the fused step
+# stores the new fp16 rows, and the block (per-token tensor, 16 tokens) or
+# group (per-channel tensor) that leaves the window at that step is sealed
+# inside the launch by the warp whose range holds it.  The steps cross
+# several seals of each tensor.
+WINDOW_CASES = [
+    # name, B, Hq, H, D, k cfg, v cfg, prefill lengths, steps, window
+    ("w_mha64_k4pc_v4pt", 2, 2, 2, 64, (4, 32, PC, ASYM), (4, 32, PT, ASYM), [300, 77], 70, 32),
+    ("w_mha64_k6pt_g64", 2, 2, 2, 64, (6, 64, PT, ASYM), (4, 64, PT, ASYM), [96, 33], 40, 16),
+    ("w_mha128_kc_vt", 2, 3, 3, 128, (2, 32, PC, ASYM), (2, 32, PT, ASYM), [95, 200], 70, 64),
+    ("w_mha128_kt_vc", 2, 3, 3, 128, (2, 32, PT, ASYM), (2, 32, PC, ASYM), [63, 190], 70, 48),
+    ("w_gqa4_128", 3, 8, 2, 128, (2, 64, PC, ASYM), (2, 64, PT, ASYM), [1000, 64, 0], 70, 128),
+    ("w_gqa8_256_pt", 1, 16, 2, 256, (4, 32, PT, ASYM), (8, 32, PT, ASYM), [700], 40, 32),
+    ("w_gqa8_256_sym6_pc", 1, 8, 1, 256, (6, 32, PC, SYM), (6, 32, PT, SYM), [333], 70, 48),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[c[0] for c in WINDOW_CASES])
+def test_fused_append_with_window(case):
+    """One launch per step for every format with a fused specialisation; the
+    cache bit-exact against the append kernel's (and the oracle's with the same
+    window), the outputs as the separate calls' and within 1e-3 of the oracle."""
+    name, B, Hq, H, D, kc, vc, n0, steps, window = case
+    wl = W(name, B, Hq, H, D, kc, vc, torch.float32, key_outlier_frac=0.02, key_outlier_scale=12.0, seed=6)
+    assert run_steps(wl, n0, steps, window=window, check_every=8) == {1}
 
 
 @pytest.mark.parametrize("bits,launches", [(1, 2), (2, 1), (3, 2)], ids=["generic", "global_combine", "generic_global"])
@@ -158,8 +186,9 @@ def test_fused_append_ragged_dead_chunks_many_steps(bits, fmt):
 
 
 def test_fused_append_falls_back_with_window():
-    """A full-precision window makes the seal of an older token part of the
-    step: the call runs the two kernels and gives the same results."""
+    """A format with no fused specialisation (two queries per kv head at
+    head_dim 64) and a full-precision window: the call runs the two kernels and
+    gives the same results."""
     wl = W("win", 2, 4, 2, 64, (4, 32, PC, ASYM), (4, 32, PT, ASYM), torch.float32, seed=8)
     T = 200
     k, v = wl.layer_kv(0, "cpu", T=T)
