@@ -130,6 +130,9 @@ CASES = [
     ("gqa8_256_sym6", 1, 8, 1, 256, (6, 32, PT, SYM), (6, 32, PT, SYM), [333]),
     ("gqa8_256_vc", 1, 8, 1, 256, (3, 64, PC, SYM), (5, 64, PC, ASYM), [300]),
     ("sym_mha64", 2, 2, 2, 64, (4, 32, PC, SYM), (2, 32, PT, SYM), [150, 31]),
+    # two queries x four value groups, one query x eight value groups (a step-scaled P operand per group)
+    ("gqa2_128_vg4", 2, 4, 2, 128, (4, 32, PC, ASYM), (4, 32, PT, ASYM), [700, 50]),
+    ("mha256_vg8", 2, 2, 2, 256, (4, 32, PT, ASYM), (5, 32, PT, ASYM), [500, 17]),
 ]
 
 
