@@ -244,6 +244,26 @@ __device__ __forceinline__ int quant_code_fast(float x, float z, float s, float 
   return min(max(q, -qmax), qmax) + (1 << (bits - 1));
 }
 
+// quant_code_fast without its division branch, for callers that test a
+// whole row of codes at once: the code is quant_code_fast's whenever `ok`
+// stays true (the quotient at most 512 and not within 2^-12 of a
+// half-integer; the caller starts `ok` from the group's test that the
+// reciprocal is normal or the step zero, with r = 0 for a zero step), and the
+// integer is read from the rounding sum's bits (1.5 * 2^23 + rint(q0) for
+// |q0| < 2^22) instead of a float-to-integer conversion.  Where `ok` turned
+// false the caller recomputes the row with quant_code_fast.
+__device__ __forceinline__ int quant_code_try(float x, float z, float r, int bits, int sym, bool& ok) {
+  const float num = sym ? x : __fsub_rn(x, z);
+  const float q0 = __fmul_rn(num, r);
+  const float m = __fadd_rn(q0, 12582912.0f);
+  const float e = __fsub_rn(q0, __fsub_rn(m, 12582912.0f));
+  ok = ok && fabsf(q0) <= 512.0f && fabsf(e) < 0.499755859375f;
+  const int q = __float_as_int(m) - 0x4B400000;
+  if (!sym) return min(max(q, 0), (1 << bits) - 1);
+  const int qmax = (1 << (bits - 1)) - 1;
+  return min(max(q, -qmax), qmax) + (1 << (bits - 1));
+}
+
 __device__ __forceinline__ int quant_code(float x, float z, float s, int bits, int sym) {
   if (s == 0.0f) return sym ? (1 << (bits - 1)) : 0;
   if (!sym) {

@@ -19,9 +19,11 @@
 //      channels and scans the G rows with fp16x2 min/max; per token, each lane
 //      owns up to 32 channels of one row and lanes sharing a group finish the
 //      reduction with shuffles.  min / max / absmax are exact in any order;
-//   3. each element's code (the step's reciprocal with the IEEE-division
-//      fallback near half-integers, quant_code_fast) is written back over its
-//      fp16 input as a 16-bit integer;
+//   3. each element's code (the step's reciprocal, quant_code_try, for a row
+//      or vector of values at once; where any of them lies near a
+//      half-integer the same values again with quant_code_fast, which takes
+//      the IEEE division there) is written back over its fp16 input as a
+//      16-bit integer;
 //   4. ldmatrix (.trans for values) delivers every lane the codes of exactly
 //      its own fragment positions of each 16-token tile (kvq_common.cuh), so
 //      each lane shifts them into its tile words and stores them with 16-byte
@@ -207,16 +209,35 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_channel_fast(Quant
     store_meta(meta, mrow + i, a.L.meta_f32, a.L.sym, z[i], s[i]);
     smax_local = fmaxf(smax_local, s[i]);
   }
-  // codes, written over the inputs as 16-bit integers
+  // codes, written over the inputs as 16-bit integers: the reciprocal rule
+  // for the lane's CPL values of a row at once, the division-checked rule
+  // for the (rare) row where any of them needs it
+  bool lane_ok = true;
+#pragma unroll
+  for (int i = 0; i < CPL; ++i) lane_ok = lane_ok && (rc[i] >= 0x1p-125f || s[i] == 0.0f);
   for (int t = 0; t < G; ++t) {
     uint32_t* row = reinterpret_cast<uint32_t*>(smp + t * row_bytes(D)) + lane * (CPL / 2);
+    float2 v[CPL / 2];
+    uint32_t w[CPL / 2];
+    bool ok = lane_ok;
 #pragma unroll
     for (int i = 0; i < CPL / 2; ++i) {
-      const float2 v = __half22float2(*reinterpret_cast<const __half2*>(row + i));
-      const uint32_t c0 = (uint32_t)quant_code_fast(v.x, z[2 * i], s[2 * i], rc[2 * i], a.L.bits, a.L.sym);
-      const uint32_t c1 = (uint32_t)quant_code_fast(v.y, z[2 * i + 1], s[2 * i + 1], rc[2 * i + 1], a.L.bits, a.L.sym);
-      row[i] = c0 | (c1 << 16);
+      v[i] = __half22float2(*reinterpret_cast<const __half2*>(row + i));
+      const uint32_t c0 = (uint32_t)quant_code_try(v[i].x, z[2 * i], rc[2 * i], a.L.bits, a.L.sym, ok);
+      const uint32_t c1 = (uint32_t)quant_code_try(v[i].y, z[2 * i + 1], rc[2 * i + 1], a.L.bits, a.L.sym, ok);
+      w[i] = c0 | (c1 << 16);
     }
+    if (!ok) {
+#pragma unroll
+      for (int i = 0; i < CPL / 2; ++i) {
+        const uint32_t c0 = (uint32_t)quant_code_fast(v[i].x, z[2 * i], s[2 * i], rc[2 * i], a.L.bits, a.L.sym);
+        const uint32_t c1 =
+            (uint32_t)quant_code_fast(v[i].y, z[2 * i + 1], s[2 * i + 1], rc[2 * i + 1], a.L.bits, a.L.sym);
+        w[i] = c0 | (c1 << 16);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < CPL / 2; ++i) row[i] = w[i];
   }
   __syncwarp();
   for (int tt = 0; tt < G / kTile; ++tt)
@@ -282,17 +303,32 @@ __global__ void __launch_bounds__(kPrefillWarps * 32) prefill_token_fast(QuantAr
         store_meta(meta, (((long)b * a.H + h) * a.tcap + (long)tile * kTile + t) * gpr + j, a.L.meta_f32, a.L.sym, z,
                    s);
       smax_local = fmaxf(smax_local, s);
+      // the reciprocal rule for 8 values at once, the division-checked rule
+      // for the (rare) vector where any of them needs it
+      const bool gok = rc >= 0x1p-125f || s == 0.0f;
       for (int k = 0; k < nv; ++k) {
-        uint4 v = src[k];
-        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+        const uint4 v = src[k];
+        const uint32_t* x = reinterpret_cast<const uint32_t*>(&v);
+        uint4 o;
+        uint32_t* w = reinterpret_cast<uint32_t*>(&o);
+        bool ok = gok;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-          const uint32_t c0 = (uint32_t)quant_code_fast(f.x, z, s, rc, a.L.bits, a.L.sym);
-          const uint32_t c1 = (uint32_t)quant_code_fast(f.y, z, s, rc, a.L.bits, a.L.sym);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x[i]));
+          const uint32_t c0 = (uint32_t)quant_code_try(f.x, z, rc, a.L.bits, a.L.sym, ok);
+          const uint32_t c1 = (uint32_t)quant_code_try(f.y, z, rc, a.L.bits, a.L.sym, ok);
           w[i] = c0 | (c1 << 16);
         }
-        src[k] = v;
+        if (!ok) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&x[i]));
+            const uint32_t c0 = (uint32_t)quant_code_fast(f.x, z, s, rc, a.L.bits, a.L.sym);
+            const uint32_t c1 = (uint32_t)quant_code_fast(f.y, z, s, rc, a.L.bits, a.L.sym);
+            w[i] = c0 | (c1 << 16);
+          }
+        }
+        src[k] = o;
       }
     } else {
       for (int k = 0; k < nv; ++k) src[k] = make_uint4(0u, 0u, 0u, 0u);

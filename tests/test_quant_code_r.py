@@ -122,3 +122,53 @@ def test_degenerate_steps_agree():
             ok = ~np.isnan(x)
             np.testing.assert_array_equal(a[ok], b[ok])
             np.testing.assert_array_equal(c[ok], b[ok])
+
+
+def code_try_rows(x, z, s, bits, sym, row=8):
+    """The prefill kernels' batched form (quant_code_try): every value through
+    the reciprocal, the integer read from the float32 bits of q0 + 1.5 * 2^23
+    (0x4B400000 + rint(q0) for |q0| < 2^22); a row of `row` consecutive values
+    in which any value fails the test (quotient beyond 512 or within 2^-12 of a
+    half-integer, or a subnormal reciprocal of a non-zero step) is recomputed
+    whole with the division-checked rule."""
+    with np.errstate(divide="ignore", invalid="ignore", over="ignore"):
+        M = F(12582912.0)
+        num = x if sym else (x - z).astype(F)
+        r = np.where(s > 0, (F(1) / s).astype(F), F(0)).astype(F)
+        q0 = (num * r).astype(F)
+        m = (q0 + M).astype(F)
+        e = (q0 - (m - M).astype(F)).astype(F)
+        q = m.view(np.int32).astype(np.int64) - 0x4B400000
+        ok = (np.abs(q0) <= F(512)) & (np.abs(e) < F(0.5 - 2.0 ** -12)) & ((r >= F(2.0 ** -125)) | (s == 0))
+        if sym:
+            qmax = (1 << (bits - 1)) - 1
+            q = np.clip(q, -qmax, qmax) + (1 << (bits - 1))
+        else:
+            q = np.clip(q, 0, (1 << bits) - 1)
+        row_ok = ok.reshape(-1, row).all(axis=1).repeat(row)
+        return np.where(row_ok, q, code_magic(x, z, s, bits, sym))
+
+
+def test_batched_rows_with_integer_bits_agree():
+    """Random groups, quotients at and around half-integers, zero steps: the
+    batched rule gives the division rule's code for every value, whether its
+    row took the fast path or was recomputed."""
+    rng = np.random.default_rng(5)
+    offsets = np.array([0.0, 2.0 ** -24, 2.0 ** -13, 2.0 ** -12, 2.0 ** -11, 0.1, 0.37])
+    offsets = np.concatenate([offsets, -offsets])
+    for bits in (2, 3, 4, 6, 8):
+        levels = (1 << bits) - 1
+        n = 256_000
+        s = fp16_steps(rng, n)
+        s[rng.integers(0, n, 500)] = F(0)
+        z = (rng.standard_normal(n) * 3).astype(np.float16).astype(F)
+        k = rng.integers(0, levels, n)
+        d = offsets[rng.integers(0, len(offsets), n)]
+        x = (z.astype(np.float64) + (k + 0.5 + d) * s.astype(np.float64)).astype(F)
+        for sym in (False, True):
+            xx = x if not sym else ((rng.integers(0, 2, n) * 2 - 1) * (k + 0.5 + d) * s.astype(np.float64)).astype(F)
+            got = code_try_rows(xx, z, s, bits, sym)
+            # a zero step codes every value as 0 (the symmetric mid-code), as the oracle does
+            want = np.where(s == 0, (1 << (bits - 1)) if sym else 0, code_div(xx, z, s, bits, sym))
+            np.testing.assert_array_equal(got, want)
+            assert (got >= 0).all() and (got <= levels).all()
