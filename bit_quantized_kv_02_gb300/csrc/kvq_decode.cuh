@@ -1532,9 +1532,14 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int grp = chunk / kCombineGroup;
   const int ngroups = (nchunks + kCombineGroup - 1) / kCombineGroup;
   const int gsize = min(kCombineGroup, nchunks - grp * kCombineGroup);
-  __threadfence();
+  // every thread's partial is written before the barrier; one thread then
+  // releases them all (the fence is cumulative over the writes the barrier
+  // ordered before it) and takes the ticket
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(tk + 1 + grp, 1u) == (unsigned)gsize - 1u;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(tk + 1 + grp, 1u) == (unsigned)gsize - 1u;
+  }
   __syncthreads();
   if (!last) return;
   __threadfence();
@@ -1614,9 +1619,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   }
   float* g0 = a.gwork + (hqb * a.max_groups + grp) * wrow;
   merge(part0, (long)max_chunks * wrow, gsize, false, g0, (long)a.max_groups * wrow);
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
+    __threadfence();
     tk[1 + grp] = 0u;
     last = atomicAdd(tk, 1u) == (unsigned)ngroups - 1u;
   }
