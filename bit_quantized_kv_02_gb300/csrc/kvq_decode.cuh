@@ -198,8 +198,8 @@ __device__ __forceinline__ void load_meta2(const char* meta, int c, int meta_f32
 // its channels once for every query, and the per-query bias partials are
 // summed by one reduce-scatter butterfly over the warp.
 template <int D, bool R8>
-__device__ __forceinline__ void build_qb(const float* qs, int rep, const char* kmeta, int kbits, int ksym, int kf32,
-                                         uint32_t* barea, float* bias, int E, float chi, int lane) {
+__device__ __forceinline__ float build_qb(const float* qs, int rep, const char* kmeta, int kbits, int ksym, int kf32,
+                                          uint32_t* barea, float* bias, int E, float chi, int lane) {
   constexpr int IT = D / 64;  // channel pairs per lane
   const float sc = exp2i(E);
   const float koff = (float)conv_off(kbits), ksoff = (float)(1 << (kbits - 1));
@@ -248,11 +248,13 @@ __device__ __forceinline__ void build_qb(const float* qs, int rep, const char* k
       }
     }
   }
+  float b1 = 0.0f;
   if (kmeta && rep == 1) {
-    float b = bpart[0];
+    // one query: the butterfly leaves the sum in every lane; the caller keeps
+    // it in a register (no shared-memory copy)
+    b1 = bpart[0];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(0xffffffffu, b, o);
-    if (lane == 0) bias[0] = b;
+    for (int o = 16; o > 0; o >>= 1) b1 += __shfl_xor_sync(0xffffffffu, b1, o);
   } else if (kmeta) {
     // reduce-scatter: after the rounds over lane bits 4, 3, 2 each lane keeps
     // one query's partial (query index from those bits), then the last two
@@ -278,6 +280,7 @@ __device__ __forceinline__ void build_qb(const float* qs, int rep, const char* k
     if ((lane & 3) == 0 && rho < rep) bias[rho] = b;
   }
   __syncwarp();
+  return b1;
 }
 
 template <int V>
@@ -768,6 +771,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int E_chan = k_token ? E_unit : norm_exp(qmax * smax_k);
   int Ek = E_unit;
   int qb_state = -1;  // query operand held: 0 unit with the key conversion's column scale, 1 plain unit, 2 key group
+  float kbias1 = 0.0f;  // one query, per-channel keys: the group's bias sum_c q_c zero'_c (query column 0's lanes)
   // conversion exponents of the key and value codes (A = 2^(g + r*rowhalf +
   // c*colhalf) * (code + off)): key columns are channels (compensated in the
   // query operand), key rows tokens (in the score fold); value rows are
@@ -933,8 +937,9 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         // cost more than the per-lane conversions, even at 8 groups a token)
       } else if ((t0 & kgmask) == 0) {
         Ek = E_chan;
-        build_qb<D, R8>(qs, rep, reinterpret_cast<const char*>(st + st_km), kbits, ksym, kf32, barea, wbias, E_chan,
-                        k_chi, lane);
+        const float b1 = build_qb<D, R8>(qs, rep, reinterpret_cast<const char*>(st + st_km), kbits, ksym, kf32, barea,
+                                         wbias, E_chan, k_chi, lane);
+        kbias1 = tig == 0 ? b1 : 0.0f;
         qb_state = 2;
         load_b();
       }
@@ -979,8 +984,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
         if (ktok) {
           load_meta(kraw, g * gs_k + jg, kf32, ksym, &kz0, &ks0);
           load_meta(kraw, (g + 8) * gs_k + jg, kf32, ksym, &kz1, &ks1);
-          kz0 = (ksym ? -ks0 * ksoff : kz0) - koff * ks0;
-          kz1 = (ksym ? -ks1 * ksoff : kz1) - koff * ks1;
+          kz0 = ksym ? -ks0 * ksoff : kz0;
+          kz1 = ksym ? -ks1 * ksoff : kz1;
+          if (koff != 0.0f) {  // (0 * step is not folded away under IEEE rules)
+            kz0 -= koff * ks0;
+            kz1 -= koff * ks1;
+          }
           ks0 *= kpost0;
           ks1 *= kpost1;
         }
@@ -991,7 +1000,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
             const int rho = min(SL::rho(q, tig), rep - 1);
             score[q] += (SL::rh(q) ? ks1 : ks0) * v + (SL::rh(q) ? kz1 : kz0) * qg[jg * rep + rho];
           } else if (kp) {
-            score[q] += v * (SL::rh(q) ? inv_e1 : inv_e0) + wbias[SL::rho(q, tig)];
+            score[q] += v * (SL::rh(q) ? inv_e1 : inv_e0) + (rep == 1 ? kbias1 : wbias[SL::rho(q, tig)]);
           } else {
             score[q] += v * inv_e0;
           }
@@ -1302,7 +1311,8 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
           float z, st;
           load_meta(vraw, tk[k] * gs_v + jg, vf32, vsym, &z, &st);
           sv[k] = st * (k < 2 ? sc_v : sc_v * v_chi);
-          zv[k] = vcen ? (vsym ? 0.0f : fmaf(vsoff, st, z)) : ((vsym ? -st * vsoff : z) - voff * st);
+          zv[k] = vcen ? (vsym ? 0.0f : fmaf(vsoff, st, z)) : (vsym ? -st * vsoff : z);
+          if (!vcen && voff != 0.0f) zv[k] -= voff * st;  // (0 * step is not folded away under IEEE rules)
         }
         make_b(pv[0] * sv[0], pv[1] * sv[1], pv[2] * sv[2], pv[3] * sv[3]);
         *zacc += pv[0] * zv[0] + pv[1] * zv[1] + pv[2] * zv[2] + pv[3] * zv[3];
