@@ -53,6 +53,11 @@ from bit_quantized_kv_02_gb300 import kvq, synth  # noqa: E402
 
 METRIC = "decode-attn achieved HBM GB/s (% of peak) and cached tokens/s on 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
+# kvq_set_decode_kernel values of the two CTA shapes the bench chooses between
+# (0: four-warp CTAs; 4: one-warp CTAs where the format has them) and their warps
+CTA_SHAPES = (0, 4)
+CTA_WARPS = {0: 4, 4: 1}
+TUNE_REPS = 2
 
 
 def workload(name: str, tokens: int = 0) -> synth.Workload:
@@ -197,7 +202,8 @@ def run_ours(args, rank, world, name):
     L = wl.layers
     steps, warm = args.steps, args.warmup
     e2e_steps = min(steps, max(3, steps // 2))
-    cap = wl.max_tokens + warm + steps + e2e_steps + 2
+    tune_steps = 2 * len(CTA_SHAPES) * TUNE_REPS  # fused steps the CTA-shape choice replays
+    cap = wl.max_tokens + warm + steps + e2e_steps + tune_steps + 2
     cfg = kvq.make_config(L, B, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v, recent_window=args.window,
                           rope_theta=args.rope)
     cache = kvq.KVQCache(cfg, device=dev)
@@ -231,25 +237,56 @@ def run_ours(args, rank, world, name):
     stream.wait_stream(torch.cuda.current_stream())
     inp.copy_(inp_all[0])
     torch.cuda.synchronize()
-    # the step: per layer the append fused into the decode launch; consecutive
-    # launches overlap their launch latency (programmatic dependent launch), so
-    # the graph holds no timing events between them
-    graph = torch.cuda.CUDAGraph()
-    launches_per_step = 0
-    with torch.cuda.graph(graph, stream=stream):
-        for l in range(L):
-            cache.kvq_append_decode_attn(l, kin[l, 0], kin[l, 1], qin[l], out[l], scale, stream=stream)
-            launches_per_step += cache.kvq_last_launches()
-    cache.kvq_refresh_lens(stream)  # capturing launched nothing
-    # the decode kernel alone: the step's L decode launches back to back (same
-    # inputs, same cache state), timed as a whole after its own L2 flush
-    graph_dec = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_dec, stream=stream):
-        for l in range(L):
-            cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = None
+
+    def capture(shape):
+        """The step graph (per layer the append fused into the decode launch;
+        consecutive launches overlap their launch latency through programmatic
+        dependent launch, so the graph holds no timing events between them) and
+        the decode kernel alone (the step's L decode launches back to back, same
+        inputs and cache state), both captured in one CTA shape."""
+        cache.kvq_set_decode_kernel(shape)
+        g = torch.cuda.CUDAGraph()
+        n = 0
+        with torch.cuda.graph(g, stream=stream):
+            for l in range(L):
+                cache.kvq_append_decode_attn(l, kin[l, 0], kin[l, 1], qin[l], out[l], scale, stream=stream)
+                n += cache.kvq_last_launches()
+        cache.kvq_refresh_lens(stream)  # capturing launched nothing
+        gd = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gd, stream=stream):
+            for l in range(L):
+                cache.kvq_decode_attn(l, qin[l], out[l], scale, stream=stream)
+        return g, gd, n
+
+    def timed_replay(g):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1)
+
+    # CTA shape of the decode launches: four-warp CTAs (the library's default)
+    # or one-warp CTAs (kvq_set_decode_kernel bit 2, where the format has that
+    # specialisation).  Which is faster depends on how the (sequence, head)
+    # ranges divide over the SMs, so each graph is timed in both shapes first
+    # (after the L2 flush, best of TUNE_REPS) and captured in the faster one.
+    tuned = {}
+    for shape in CTA_SHAPES:
+        g, gd, n = capture(shape)
+        ts = min(timed_replay(g) for _ in range(TUNE_REPS))
+        td = min(timed_replay(gd) for _ in range(TUNE_REPS))
+        tuned[shape] = (ts, td)
+        del g, gd
+    step_shape = min(CTA_SHAPES, key=lambda x: tuned[x][0])
+    dec_shape = min(CTA_SHAPES, key=lambda x: tuned[x][1])
+    graph, _, launches_per_step = capture(step_shape)
+    _, graph_dec, _ = capture(dec_shape)
+    cache.kvq_refresh_lens(stream)
 
     def traffic():
         cache.kvq_refresh_lens(stream)
@@ -368,6 +405,12 @@ def run_ours(args, rank, world, name):
                        "k_format": "bits,group,axis(0 per-token,1 per-channel),mode(0 asym,1 sym)",
                        "step": "per layer: kvq_append_decode_attn (append fused into the decode launch; CUDA graph)",
                        "l2": "256 MB buffer written before every timed step (L2 flushed)",
+                       "cta_warps": {"step": CTA_WARPS[step_shape], "decode": CTA_WARPS[dec_shape],
+                                     "choice": "each graph timed in both CTA shapes (best of "
+                                               f"{TUNE_REPS} after an L2 flush) before the warm-up; "
+                                               "the faster captured",
+                                     "ms_step": {CTA_WARPS[x]: round(tuned[x][0], 4) for x in CTA_SHAPES},
+                                     "ms_decode": {CTA_WARPS[x]: round(tuned[x][1], 4) for x in CTA_SHAPES}},
                        "parallelism": f"dp{world} (sequences sharded, no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": None,

@@ -417,9 +417,10 @@ kvq_status kvq_set_decode_plan(kvq_cache_t C, int plan_tokens) {
 }
 
 kvq_status kvq_set_decode_kernel(kvq_cache_t C, int which) {
-  if (!C || which < 0 || which > 3) return KVQ_ERR_INVALID_ARG;
+  if (!C || which < 0 || which > 7) return KVQ_ERR_INVALID_ARG;
   C->generic_decode = which & 1;
   C->global_combine = (which >> 1) & 1;
+  C->one_warp = (which >> 2) & 1;
   return cuda_status(C, decode_setup(C));
 }
 

@@ -75,7 +75,7 @@ int window_weight(const kvq_cache* C) {
 }  // namespace
 
 // Shared-memory plan and per-call split of the token range.
-static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
+static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out, int nw = kWarps) {
   const kvq_config& cfg = C->cfg;
   const int D = cfg.head_dim, rep = cfg.q_heads / cfg.kv_heads;
   const bool r8 = rep == 8;
@@ -138,7 +138,7 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
   a.stage_off = L.stage_off;
   a.warp_bytes = L.warp_bytes;
   a.head_bytes = L.head_bytes;
-  P->smem = (size_t)a.head_bytes + (size_t)kWarps * a.warp_bytes;
+  P->smem = (size_t)a.head_bytes + (size_t)nw * a.warp_bytes;
   if (!C->dec_fn) return cudaErrorInvalidValue;
   *occ_out = C->dec_occ;
   return cudaSuccess;
@@ -147,14 +147,17 @@ static cudaError_t make_plan(kvq_cache* C, int layer, Plan* P, int* occ_out) {
 cudaError_t decode_setup(kvq_cache* C) {
   // pre-RoPE caches run the rotary instances of the runtime-format kernel
   const bool rope = C->cfg.rope_theta > 0.0f;
-  void* fn = C->generic_decode ? nullptr : (rope ? decode_kernel_rope_fast(C) : decode_kernel_fast(C));
+  int nw = kWarps;
+  void* fn = C->generic_decode ? nullptr : (rope ? decode_kernel_rope_fast(C) : decode_kernel_fast(C, &nw));
+  if (!fn) nw = kWarps;
   if (!fn && rope) fn = pick_kernel_rope(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
   if (!fn) fn = pick_kernel(C->cfg.head_dim, C->cfg.q_heads / C->cfg.kv_heads == 8, C->v.axis);
   if (!fn) return cudaErrorInvalidValue;
   C->dec_fn = fn;
+  C->dec_nw = nw;
   Plan P;
   int occ = 1;
-  cudaError_t e = make_plan(C, 0, &P, &occ);
+  cudaError_t e = make_plan(C, 0, &P, &occ, nw);
   if (e != cudaSuccess) return e;
   if (P.smem > 227 * 1024) return cudaErrorInvalidValue;
   e = raise_smem_limit(fn, P.smem);
@@ -163,12 +166,14 @@ cudaError_t decode_setup(kvq_cache* C) {
   // alternating append / decode launches need no L1 / shared reconfiguration
   e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kWarps * 32, P.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, nw * 32, P.smem);
   if (e != cudaSuccess) return e;
   C->dec_smem = P.smem;
   C->dec_occ = std::max(occ, 1);
   const int rep = C->cfg.q_heads / C->cfg.kv_heads;
-  C->dec_cluster_ok = !C->global_combine && cluster_fits(fn, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
+  // (one-warp CTAs merge through the global workspace only)
+  C->dec_cluster_ok = !C->global_combine && nw == kWarps &&
+                      cluster_fits(fn, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
   // the fused append needs a fused specialisation, layouts where each
   // (sequence, head) owns all it writes (no whole-vector groups; with a
   // window the block or group leaving it is sealed by the warp whose range
@@ -176,32 +181,45 @@ cudaError_t decode_setup(kvq_cache* C) {
   // kernel's residency and cluster merge (the launch is planned for the plain kernel)
   const int ring = (1 << P.a.lg_nstages) * P.a.stage_bytes;
   C->fused_ok = 0;
-  C->dec_fn_fused = (C->generic_decode || rope) ? nullptr : decode_kernel_fused(C);
+  int nwf = kWarps;
+  C->dec_fn_fused = (C->generic_decode || rope) ? nullptr : decode_kernel_fused(C, &nwf);
+  C->dec_nw_fused = nwf;
   const int window = C->k.window || C->v.window;
   if (C->dec_fn_fused && !C->k.whole && !C->v.whole &&
       fused_append_scratch(C->cfg.head_dim, C->k.axis, C->v.axis, window) <= ring) {
     void* ff = C->dec_fn_fused;
-    int occ_f = 0;
-    e = raise_smem_limit(ff, P.smem);
+    Plan Pf;
+    int occ_f = 0, occ_unused = 1;
+    e = make_plan(C, 0, &Pf, &occ_unused, nwf);
+    if (e == cudaSuccess) e = raise_smem_limit(ff, Pf.smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(ff, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_f, ff, kWarps * 32, P.smem);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_f, ff, nwf * 32, Pf.smem);
     if (e != cudaSuccess) return e;
-    const bool cl_same =
-        !C->dec_cluster_ok || cluster_fits(ff, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
-    C->fused_ok = occ_f >= C->dec_occ && cl_same;
+    C->dec_occ_fused = std::max(occ_f, 1);
+    if (nwf == nw) {
+      // same CTA shape: planned like the plain kernel, whose residency and cluster merge it must keep
+      const bool cl_same =
+          !C->dec_cluster_ok || cluster_fits(ff, P.smem, rep, C->cfg.head_dim, C->dec_occ, P.a.warp_bytes);
+      C->fused_ok = occ_f >= C->dec_occ && cl_same;
+    } else {
+      C->fused_ok = occ_f > 0;  // planned for its own residency, merged through the global workspace
+    }
   }
   return cudaSuccess;
 }
 
-// Choose tokens per CTA (a multiple of 4 warps x the alignment unit) so that
+// Choose tokens per CTA (a multiple of nw warps x the alignment unit) so that
 // the CTAs fill whole waves of the GPU with as little imbalance as possible.
 // Cost = waves x (tokens per CTA + a fixed cost per CTA).  The fixed cost (the
-// prologue's first-data latency, the split-K merge) is worth about 384 tokens
-// of streaming: on a Llama-2-13B-shaped batch (16 x 40 heads x 4113 tokens)
-// three splits of 1408 tokens ran 13 % faster than seven of 640.  Candidates
-// are even fractions of the whole job and even splits of the longest
-// sequence.
-static int choose_split(const kvq_cache* C, const int32_t* lens, int unit, int slots, int max_chunks) {
+// prologue's first-data latency, the split-K merge) is worth about 96 tokens
+// of streaming per warp of the CTA: on a Llama-2-13B-shaped batch (16 x 40
+// heads x 4113 tokens) three splits of 1408 tokens in four-warp CTAs ran 13 %
+// faster than seven of 640.  Candidates are even fractions of the whole job
+// and even splits of the longest sequence.
+static int choose_split(const kvq_cache* C, const int32_t* lens, int unit, int slots, int max_chunks,
+                        int nw = kWarps) {
+  const int step = nw * unit;
+  const double fixed = 96.0 * nw;
   const int B = C->cfg.batch, H = C->cfg.kv_heads;
   long total = 0;
   int maxn = 0;
@@ -209,8 +227,8 @@ static int choose_split(const kvq_cache* C, const int32_t* lens, int unit, int s
     total += lens[b];
     maxn = std::max(maxn, (int)lens[b]);
   }
-  if (maxn == 0) return 4 * unit;
-  const int s_min_cap = round_up((maxn + max_chunks - 1) / max_chunks, 4 * unit);
+  if (maxn == 0) return step;
+  const int s_min_cap = round_up((maxn + max_chunks - 1) / max_chunks, step);
   int best = 0;
   double best_cost = 1e300;
   auto eval = [&](int S) {
@@ -219,16 +237,16 @@ static int choose_split(const kvq_cache* C, const int32_t* lens, int unit, int s
     for (int b = 0; b < B; ++b) ctas += (lens[b] + S - 1) / S;
     ctas *= H;
     const double waves = std::ceil((double)ctas / slots);
-    const double cost = waves * (S + 384.0);
+    const double cost = waves * (S + fixed);
     if (cost < best_cost - 1e-9 || (std::fabs(cost - best_cost) < 1e-9 && S > best)) {
       best_cost = cost;
       best = S;
     }
   };
   const double ideal = (double)total * H / slots;
-  for (int k = 1; k <= 4096; k *= 2) eval(4 * unit * k);
-  for (int m = 1; m <= 8; ++m) eval(round_up((int)std::ceil(ideal / m), 4 * unit));
-  for (int n = 1; n <= 64; ++n) eval(round_up((maxn + n - 1) / n, 4 * unit));
+  for (int k = 1; k <= 4096; k *= 2) eval(step * k);
+  for (int m = 1; m <= 8; ++m) eval(round_up((int)std::ceil(ideal / m), step));
+  for (int n = 1; n <= 64; ++n) eval(round_up((maxn + n - 1) / n, step));
   return best;
 }
 
@@ -237,9 +255,11 @@ static int choose_split(const kvq_cache* C, const int32_t* lens, int unit, int s
 // split size, grid, and how the split-K partials merge.
 static cudaError_t plan_launch(kvq_cache* C, int layer, const void* q, int q_f32, float scale, float* out, Plan* P,
                                dim3* grid, bool fused = false) {
+  const int nw = fused ? C->dec_nw_fused : C->dec_nw;
   int occ = 1;
-  cudaError_t e = make_plan(C, layer, P, &occ);
+  cudaError_t e = make_plan(C, layer, P, &occ, nw);
   if (e != cudaSuccess) return e;
+  if (fused && nw != C->dec_nw) occ = C->dec_occ_fused;
   DecodeArgs& a = P->a;
   const kvq_config& cfg = C->cfg;
   int unit = kTile;
@@ -266,9 +286,12 @@ static cudaError_t plan_launch(kvq_cache* C, int layer, const void* q, int q_f32
   // one split of 4224 tokens per (sequence, head), one wave of 640 CTAs, 5 %
   // faster per step than three splits of 1408, while the plain decode is 4 %
   // slower that way)
-  const int slots = C->sm_count * (fused ? occ : std::min(occ, 4));
-  a.S = choose_split(C, plan.data(), unit, slots, C->max_chunks);
-  a.Sw = a.S / kWarps;
+  // (in warps: about 16 resident warps per SM; the four-warp fused launch
+  // takes every resident CTA)
+  const int slots =
+      C->sm_count * ((fused && nw == kWarps) ? occ : std::max(1, std::min(occ * nw, 4 * kWarps) / nw));
+  a.S = choose_split(C, plan.data(), unit, slots, C->max_chunks, nw);
+  a.Sw = a.S / nw;
   int maxn = 0;
   for (int b = 0; b < cfg.batch; ++b) maxn = std::max(maxn, (int)plan[b]);
   const int nch = std::max(1, (maxn + a.S - 1) / a.S);
@@ -278,7 +301,7 @@ static cudaError_t plan_launch(kvq_cache* C, int layer, const void* q, int q_f32
   // (only when the whole grid is resident at once: with several waves, CTAs
   // that wait for their cluster would hold slots that later CTAs need)
   const long ctas = (long)nch * cfg.kv_heads * cfg.batch;
-  a.csize = (C->dec_cluster_ok && nch <= kMaxCluster && ctas <= slots) ? nch : 0;
+  a.csize = (C->dec_cluster_ok && nw == kWarps && nch <= kMaxCluster && ctas <= slots) ? nch : 0;
   a.gath_off = (int)P->smem;
   P->smem += gather_bytes(a.csize, cfg.q_heads / cfg.kv_heads, cfg.head_dim);
   a.q = q;
@@ -296,7 +319,7 @@ cudaError_t launch_decode(kvq_cache* C, int layer, const void* q, int q_f32, flo
   cudaError_t e = plan_launch(C, layer, q, q_f32, scale, out, &P, &grid);
   if (e != cudaSuccess) return e;
   void* args[] = {&P.a};
-  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), P.smem, st, args, P.a.csize);
+  e = launch_pdl(C->dec_fn, grid, dim3(C->dec_nw * 32), P.smem, st, args, P.a.csize);
   ++*launches;
   return e;
 }
@@ -311,7 +334,7 @@ cudaError_t launch_append_decode(kvq_cache* C, int layer, const void* k, const v
   if (e != cudaSuccess) return e;
   P.a.ap = make_append_args(C, layer, k, v, x_f32);
   void* args[] = {&P.a};
-  e = launch_pdl(C->dec_fn_fused, grid, dim3(kWarps * 32), P.smem, st, args, P.a.csize);
+  e = launch_pdl(C->dec_fn_fused, grid, dim3(C->dec_nw_fused * 32), P.smem, st, args, P.a.csize);
   ++*launches;
   return e;
 }
@@ -330,7 +353,7 @@ cudaError_t launch_decode_scratch(kvq_cache* C, int layer, const void* q, int q_
   a.gwork = work + (size_t)C->cfg.batch * C->cfg.q_heads * C->max_chunks * (C->cfg.head_dim + 4);
   a.tickets = tickets;
   void* args[] = {&a};
-  e = launch_pdl(C->dec_fn, grid, dim3(kWarps * 32), P.smem, st, args, a.csize);
+  e = launch_pdl(C->dec_fn, grid, dim3(C->dec_nw * 32), P.smem, st, args, a.csize);
   ++*launches;
   return e;
 }

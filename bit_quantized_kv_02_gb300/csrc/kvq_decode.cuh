@@ -300,6 +300,7 @@ struct StageR {
 // (the generic kernel, any format the C ABI accepts).
 struct DynCfg {
   static constexpr int kStaticStages = 0;  // stage count known only at run time
+  static constexpr int kRep = 8;           // largest query heads per KV head
   static constexpr int kRope = 1;          // (layouts come from the launch arguments)
   __device__ static int rep(const DecodeArgs& a) { return a.rep; }
   __device__ static int kbits(const DecodeArgs& a) { return a.K.bits; }
@@ -350,6 +351,7 @@ struct StatCfg {
   static constexpr int kRope = ROPEL;  // the layout includes the rotary tables
   static constexpr DecLayout L = dec_layout(D, REP, KB, KAX, 0, KGPT, KMB, VB, VAX, 0, VGPT, VMB, 0, ROPEL);
   static constexpr int kStaticStages = 1 << L.lg_ns;
+  static constexpr int kRep = REP;
   __device__ static constexpr int rep(const DecodeArgs&) { return REP; }
   __device__ static constexpr int kbits(const DecodeArgs&) { return KB; }
   __device__ static constexpr int ksym(const DecodeArgs&) { return KSYM; }
@@ -399,11 +401,16 @@ __host__ __device__ constexpr int decode_min_blocks(int D, bool is_static, int v
 
 // FUSED: the launch also appends the new token (kvq_append_decode_attn); the
 // plain decode kernel is compiled without any of that code.
+// NW: warps per CTA (each warp streams its own token range; the CTA's warps
+// merge in shared memory).  One-warp CTAs let the block scheduler spread the
+// warps of a launch over the SMs one at a time.
 // ROPE: the keys are cached before the rotary position embedding; every
 // dequantized key is turned by its token's angles before the QK MMA (runtime
 // formats, and compile-time configurations built with the rotary layout).
-template <int D, bool R8, int VAXIS, class CFG, bool FUSED = false, bool ROPE = false>
-__global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages != 0, VAXIS, ROPE)) decode_kernel(const __grid_constant__ DecodeArgs a) {
+template <int D, bool R8, int VAXIS, class CFG, bool FUSED = false, bool ROPE = false, int NW = kWarps>
+__global__ void __launch_bounds__(NW * 32, decode_min_blocks(D, CFG::kStaticStages != 0, VAXIS, ROPE) * kWarps / NW)
+    decode_kernel(const __grid_constant__ DecodeArgs a) {
+  static_assert(NW == kWarps || !ROPE, "the rotary tables are built by four warps");
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NCH = D / 16;                // 16-channel chunks / m-tiles
   constexpr int NB = R8 ? 2 : 1;             // B operands per chunk (hi/lo split over two MMAs)
@@ -424,11 +431,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
   const int hq0 = h * rep;
   // the query and the largest steps are requested before the length, so the
   // three loads are in flight together
-  constexpr int QPT = D / 16;  // query values per thread at rep 8
+  // query values per thread (four warps: rep 8)
+  constexpr int QPT = NW == kWarps ? D / 16 : (CFG::kRep * D + NW * 32 - 1) / (NW * 32);
   float qv[QPT];
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {
-    const int i = threadIdx.x + u * 128;
+    const int i = threadIdx.x + u * (NW * 32);
     const long qi = ((long)b * H * rep + hq0) * D + i;
     qv[u] = 0.0f;
     if (i < rep * D)
@@ -668,7 +676,7 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
 
 #pragma unroll
   for (int u = 0; u < QPT; ++u) {
-    const int i = threadIdx.x + u * 128;
+    const int i = threadIdx.x + u * (NW * 32);
     if (i < rep * D) qs[i] = qv[u] * a.scale_log2;
   }
   // rotary tables: pair frequencies theta_i = base^(-2i/D) as fp32 (hi, lo)
@@ -1493,12 +1501,12 @@ __global__ void __launch_bounds__(128, decode_min_blocks(D, CFG::kStaticStages !
     const int rho = i / rowlen, c = i % rowlen;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mw[(w * rep + rho) * rowlen + D]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, mw[(w * rep + rho) * rowlen + D]);
     float acc = 0.0f;
     if (c == D) acc = M;
     else {
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float mwv = mw[(w * rep + rho) * rowlen + D];
         const float f = (mwv == -INFINITY) ? 0.0f : fast_exp2(mwv - M);
         acc += f * mw[(w * rep + rho) * rowlen + c];

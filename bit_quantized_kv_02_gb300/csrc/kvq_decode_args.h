@@ -154,11 +154,10 @@ void* decode_kernel_ptr_rope_d64(bool r8, int vaxis);
 void* decode_kernel_ptr_rope_d128(bool r8, int vaxis);
 void* decode_kernel_ptr_rope_d256(bool r8, int vaxis);
 
-// compile-time specialisation for this cache's formats, or null (generic kernel)
-void* decode_kernel_fast(const kvq_cache* C);
-// the second part of the specialisation table (plain and fused)
-void* decode_kernel_fast_part1(const kvq_cache* C);
-void* decode_kernel_fused_part1(const kvq_cache* C);
+// the second part of the compile-time specialisation table (plain and fused;
+// decode_kernel_fast / decode_kernel_fused search both parts)
+void* decode_kernel_fast_part1(const kvq_cache* C, int* nw);
+void* decode_kernel_fused_part1(const kvq_cache* C, int* nw);
 // compile-time specialisation of the rotary decode kernel for this cache, or null
 void* decode_kernel_rope_fast(const kvq_cache* C);
 

@@ -5,9 +5,9 @@
 
 namespace kvq {
 
-void* decode_kernel_fast(const kvq_cache* C) {
-  void* fn = lookup_specialised<false, 0>(C);
-  return fn ? fn : decode_kernel_fast_part1(C);
+void* decode_kernel_fast(const kvq_cache* C, int* nw) {
+  void* fn = lookup_specialised<false, 0>(C, nw);
+  return fn ? fn : decode_kernel_fast_part1(C, nw);
 }
 
 }  // namespace kvq

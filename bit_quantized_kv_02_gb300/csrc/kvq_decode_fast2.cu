@@ -4,7 +4,7 @@
 
 namespace kvq {
 
-void* decode_kernel_fast_part1(const kvq_cache* C) { return lookup_specialised<false, 1>(C); }
+void* decode_kernel_fast_part1(const kvq_cache* C, int* nw) { return lookup_specialised<false, 1>(C, nw); }
 
 void* decode_kernel_rope_fast(const kvq_cache* C) { return lookup_specialised_rope(C); }
 

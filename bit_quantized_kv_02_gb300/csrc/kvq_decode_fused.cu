@@ -6,9 +6,9 @@
 
 namespace kvq {
 
-void* decode_kernel_fused(const kvq_cache* C) {
-  void* fn = lookup_specialised<true, 0>(C);
-  return fn ? fn : decode_kernel_fused_part1(C);
+void* decode_kernel_fused(const kvq_cache* C, int* nw) {
+  void* fn = lookup_specialised<true, 0>(C, nw);
+  return fn ? fn : decode_kernel_fused_part1(C, nw);
 }
 
 }  // namespace kvq

@@ -4,6 +4,6 @@
 
 namespace kvq {
 
-void* decode_kernel_fused_part1(const kvq_cache* C) { return lookup_specialised<true, 1>(C); }
+void* decode_kernel_fused_part1(const kvq_cache* C, int* nw) { return lookup_specialised<true, 1>(C, nw); }
 
 }  // namespace kvq

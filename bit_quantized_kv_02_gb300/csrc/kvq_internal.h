@@ -34,6 +34,10 @@ struct kvq_cache {
   int generic_decode = 0;  // 1: always use the generic (runtime-format) decode kernel
   int fused_ok = 0;        // the append can run inside the decode launch (kvq_append_decode_attn)
   void* dec_fn_fused = nullptr;  // the decode kernel's specialisation with the append fused in
+  int dec_nw = kvq::kWarps;        // warps per CTA of dec_fn
+  int dec_nw_fused = kvq::kWarps;  // warps per CTA of dec_fn_fused
+  int dec_occ_fused = 1;           // resident CTAs per SM of dec_fn_fused
+  int one_warp = 0;                // 1: one-warp-CTA specialisations where a format has them
   uint32_t* d_arrive = nullptr;  // [batch][kv_heads] arrival counters of the fused append
 };
 
@@ -97,8 +101,9 @@ cudaError_t prefill_fast_setup();
 // one-time kernel attribute set-up at cache creation (keeps launches capturable)
 cudaError_t quant_setup(kvq_cache* C);
 cudaError_t decode_setup(kvq_cache* C);
-void* decode_kernel_fast(const kvq_cache* C);
-void* decode_kernel_fused(const kvq_cache* C);
+// (nw, if not null, receives the kernel's warps per CTA)
+void* decode_kernel_fast(const kvq_cache* C, int* nw = nullptr);
+void* decode_kernel_fused(const kvq_cache* C, int* nw = nullptr);
 void* decode_kernel_rope_fast(const kvq_cache* C);
 
 // decode: plans the split, launches the split-K kernel (which also combines)

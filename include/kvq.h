@@ -277,15 +277,18 @@ kvq_status kvq_device_status(kvq_cache_t cache, void* stream);
  * lengths. */
 kvq_status kvq_set_decode_plan(kvq_cache_t cache, int plan_tokens);
 
-/* Decode kernel choice, two bits.  Bit 0: 0 (default) uses a compile-time
+/* Decode kernel choice, three bits.  Bit 0: 0 (default) uses a compile-time
  * specialisation of the decode kernel when the cache's formats match one (fp16
  * metadata, no whole-vector groups, formats of the benchmarked workloads), else
  * the generic kernel; 1 always uses the generic (runtime-format) kernel.
  * Bit 1: 0 (default) merges the split-K partials of a (sequence, kv head)
  * inside one thread-block cluster when there are at most 8 splits (through
  * distributed shared memory), else through the global workspace; 1 always uses
- * the global workspace.  Every choice computes the same result (up to fp32
- * summation order); they only affect speed.  which outside 0..3:
+ * the global workspace.  Bit 2: 1 uses one-warp CTAs (each CTA streams one
+ * token range; the ranges of a (sequence, kv head) merge through the global
+ * workspace) where a compile-time specialisation exists in that shape, 0
+ * (default) four-warp CTAs.  Every choice computes the same result (up to fp32
+ * summation order); they only affect speed.  which outside 0..7:
  * KVQ_ERR_INVALID_ARG. */
 kvq_status kvq_set_decode_kernel(kvq_cache_t cache, int which);
 
