@@ -21,11 +21,14 @@ Between timed steps a 256 MB buffer is written to flush the 126 MB L2.
           from kvq_decode_traffic) per step / device time of the step, inputs
           already resident in HBM (the step's new tokens and queries are copied
           device-to-device into the graph's input buffers inside the timed region)
-  e2e   : same metric with the inputs copied from pinned host memory and the
-          outputs copied back to pinned host memory inside the timed region
+  e2e   : same metric with every step's inputs copied from pinned host memory
+          and its outputs copied back to pinned host memory inside the timed
+          region (the steps enqueued back to back)
   roofline : decode kernel alone; CUDA events on the launching stream around a
           graph of the step's decode launches.  `traffic` is null: the DRAM
           byte counts come from separate ncu captures (see profiles/).
+  config.cta_warps : the CTA shape of each graph (four-warp CTAs, or one-warp
+          CTAs where the format has them), the faster of the two timed first.
 `--phase prefill` times kvq_prefill_quantize instead (fp16 keys and values of
 every layer in HBM -> packed codes, metadata and fp16 tails): bytes = fp16
 input read + codes, metadata and tail written.
@@ -113,39 +116,25 @@ class _Nvml:
 
 
 class Clocks:
-    """SM clock / clock-event-reason sampler running during the timed region:
-    NVML polled from a thread every 0.2 ms (the timed regions last only
-    milliseconds), else nvidia-smi every 200 ms."""
+    """SM clock / clock-event-reason sampler for the timed region: one NVML
+    sample from the calling thread once a step is enqueued, while the GPU runs
+    it (no sampler thread competing with the host while it enqueues a step
+    between its timing events, and no back-to-back driver queries while the
+    GPU works), else nvidia-smi every 200 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, dev: torch.device):
-        import threading
         self.proc = None
         self.samples = []
-        self.switch = sys.getswitchinterval()
-        self.stop_flag = threading.Event()
-        self.thread = None
         self.nv = None
         try:
-            nv = _Nvml(dev)
-            self.nv = nv
-
-            def loop():
-                while not self.stop_flag.is_set():
-                    r = nv.sample()
-                    if r is not None:
-                        self.samples.append(r)
-                    time.sleep(0.0002)
-
-            sys.setswitchinterval(0.0002)  # let the sampler run while the host waits on the GPU
-            self.thread = threading.Thread(target=loop, daemon=True)
-            self.thread.start()
-            self.source = "nvml, polled every 0.2 ms"
+            self.nv = _Nvml(dev)
+            self.source = "nvml, one sample while each timed step runs"
             return
         except Exception:
-            self.thread = None
+            self.nv = None
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={dev.index or 0}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -155,18 +144,17 @@ class Clocks:
             self.proc = None
 
     def poll(self):
-        """One sample from the calling thread (used while the GPU runs a step)."""
-        if self.nv is not None:
-            r = self.nv.sample()
-            if r is not None:
-                self.samples.append(r)
+        """One sample from the calling thread (called while the GPU runs a step)."""
+        if self.nv is None:
+            return
+        r = self.nv.sample()
+        if r is not None:
+            self.samples.append(r)
 
     def stop(self):
-        if self.thread is not None:
-            self.stop_flag.set()
-            self.thread.join(timeout=5)
-            sys.setswitchinterval(self.switch)
-        elif self.proc:
+        if self.nv is None and not self.proc:
+            return None
+        if self.nv is None:
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -183,8 +171,6 @@ class Clocks:
                                          [n for n, v in zip(names, f[5:9]) if v.lower().startswith("active")]))
                 except ValueError:
                     continue
-        else:
-            return None
         if not self.samples:
             return None
         sm = [x[0] for x in self.samples]
@@ -203,7 +189,7 @@ def run_ours(args, rank, world, name):
     steps, warm = args.steps, args.warmup
     e2e_steps = min(steps, max(3, steps // 2))
     tune_steps = 2 * len(CTA_SHAPES) * TUNE_REPS  # fused steps the CTA-shape choice replays
-    cap = wl.max_tokens + warm + steps + e2e_steps + tune_steps + 2
+    cap = wl.max_tokens + warm + steps + 2 * e2e_steps + tune_steps + 2
     cfg = kvq.make_config(L, B, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v, recent_window=args.window,
                           rope_theta=args.rope)
     cache = kvq.KVQCache(cfg, device=dev)
@@ -231,7 +217,8 @@ def run_ours(args, rank, world, name):
     kin = inp[:nk].view(L, 2, B, H, D)
     qin = inp[nk:].view(L, B, Hq, D)
     out = torch.empty((L, B, Hq, D), dtype=torch.float32, device=dev)
-    out_host = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    # pinned host buffers for the end-to-end steps' outputs (one per step)
+    out_host = torch.empty((max(e2e_steps, 1),) + tuple(out.shape), dtype=torch.float32).pin_memory()
     scale = float(np.float32(1.0 / np.sqrt(D)))
     stream = torch.cuda.Stream(device=dev)
     stream.wait_stream(torch.cuda.current_stream())
@@ -293,17 +280,12 @@ def run_ours(args, rank, world, name):
         return sum(cache.kvq_decode_traffic(l, kvq.F16) for l in range(L)), \
             sum(sum(cache.kvq_get_lens(l)) for l in range(L))
 
-    def one_step(s, e2e: bool):
+    def one_step(s):
         with torch.cuda.stream(stream):
             flush.zero_()
             e0.record(stream)
-            if e2e:
-                inp.copy_(inp_host[s], non_blocking=True)
-            else:
-                inp.copy_(inp_all[s], non_blocking=True)
+            inp.copy_(inp_all[s], non_blocking=True)
             graph.replay()
-            if e2e:
-                out_host.copy_(out, non_blocking=True)
             e1.record(stream)
         if clocks:
             clocks.poll()  # the GPU is running the step now
@@ -323,13 +305,13 @@ def run_ours(args, rank, world, name):
 
     # warm-up (untimed)
     for s in range(warm):
-        one_step(s, False)
+        one_step(s)
         decode_pass()
     kdist.barrier()
     clocks = Clocks(dev) if rank == 0 else None
     t_steps, t_decode, tot_bytes, tot_tokens = 0.0, 0.0, 0.0, 0.0
     for s in range(warm, nsteps):
-        t_steps += one_step(s, False)
+        t_steps += one_step(s)
         by, tk = traffic()
         tot_bytes += by
         tot_tokens += tk
@@ -368,11 +350,30 @@ def run_ours(args, rank, world, name):
                "path": "per layer: kvq_dequantize (packed -> fp16 rows) + kvq_decode_attn_materialized",
                "fp16_bytes_written_and_read_per_layer": 2 * 2 * sum(wl.lens) * H * D * 2}
         del k16, v16
-    # end-to-end: host inputs -> device -> host outputs, same graph
-    t_e2e = 0.0
-    for s in range(e2e_steps):
-        t_e2e += one_step(warm + s, True)
-    by_e2e = traffic()[0] * e2e_steps if e2e_steps else 0.0
+    # End to end: every step copies its inputs from pinned host memory to the
+    # device, replays the step graph and copies its outputs back into a pinned
+    # host buffer of its own.  The steps are enqueued back to back between one
+    # pair of events, so the GPU runs them in order while the host enqueues the
+    # next one: a host-side stall while a copy is being enqueued (measured: now
+    # and then 1.5 ms, when each step sat between its own events) does not
+    # count as GPU time.  The cache is far larger than L2, so no flush between
+    # the steps.  The sequence runs once untimed first (the first copies from
+    # and to pinned buffers in a process cost extra).
+    t_e2e, by_e2e = 0.0, 0.0
+    if e2e_steps:
+        for timed in (False, True):
+            by0 = traffic()[0]
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                e0.record(stream)
+                for s in range(e2e_steps):
+                    inp.copy_(inp_host[warm + s], non_blocking=True)
+                    graph.replay()
+                    out_host[s].copy_(out, non_blocking=True)
+                e1.record(stream)
+            stream.synchronize()
+            t_e2e = e0.elapsed_time(e1)
+            by_e2e = 0.5 * (by0 + traffic()[0]) * e2e_steps
     # correctness guard: the device reported no timed-out wait
     st = cache.kvq_device_status(stream)
     if st != 0:
@@ -424,7 +425,8 @@ def run_ours(args, rank, world, name):
             "gpu_launches": launches_per_step * steps,
             "e2e": {"value": round(bytes_e2e_all / (t_e2e_max * 1e-3) / 1e9, 2) if e2e_steps else None,
                     "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-                    "path": "pinned host -> device copies, graph of kvq_append_decode_attn, device -> host"},
+                    "path": "per step: pinned host -> device copy of the inputs, graph of kvq_append_decode_attn, "
+                            "device -> pinned host copy of the outputs; steps enqueued back to back"},
             "clocks": clk,
         }
         if mat is not None:
@@ -465,9 +467,12 @@ def run_prefill(args, rank, world, name):
                 cache.kvq_prefill_quantize(l, k, v, wl.lens, stream=stream)
                 launches += cache.kvq_last_launches()
             e1.record(stream)
+        if clocks:
+            clocks.poll()  # the GPU is running the layers now
         stream.synchronize()
         return e0.elapsed_time(e1)
 
+    clocks = None
     for _ in range(warm):
         one_step()
     kdist.barrier()
@@ -475,8 +480,6 @@ def run_prefill(args, rank, world, name):
     t = 0.0
     for _ in range(steps):
         t += one_step()
-        if clocks:
-            clocks.poll()
     clk = clocks.stop() if clocks else None
     kdist.barrier()
     # end to end: the layer's fp16 inputs copied from pinned host memory inside the timed region
