@@ -424,6 +424,12 @@ kvq_status kvq_set_decode_kernel(kvq_cache_t C, int which) {
   return cuda_status(C, decode_setup(C));
 }
 
+int kvq_decode_cta_warps(kvq_cache_t C, int fused) {
+  if (!C || !C->dec_fn) return 0;
+  if (fused) return C->fused_ok ? C->dec_nw_fused : 0;
+  return C->dec_nw;
+}
+
 int kvq_decode_kernel_specialized(kvq_cache_t C) {
   if (!C || !C->dec_fn || C->generic_decode) return 0;
   void* fast = C->cfg.rope_theta > 0.0f ? decode_kernel_rope_fast(C) : decode_kernel_fast(C);

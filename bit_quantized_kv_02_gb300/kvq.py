@@ -59,7 +59,7 @@ EXPORTED = ["kvq_cache_bytes", "kvq_cache_create", "kvq_cache_destroy", "kvq_pre
             "kvq_device_status", "kvq_last_launches", "kvq_status_string", "kvq_last_error",
             "kvq_set_decode_plan", "kvq_refresh_lens", "kvq_decode_attn_static", "kvq_set_decode_kernel",
             "kvq_decode_kernel_specialized", "kvq_dequantize", "kvq_decode_attn_materialized",
-            "kvq_append_decode_attn"]
+            "kvq_append_decode_attn", "kvq_decode_cta_warps"]
 
 
 def lib():
@@ -96,6 +96,8 @@ def lib():
         L.kvq_set_decode_kernel.argtypes = [P, I]
         L.kvq_decode_kernel_specialized.argtypes = [P]
         L.kvq_decode_kernel_specialized.restype = I
+        L.kvq_decode_cta_warps.argtypes = [P, I]
+        L.kvq_decode_cta_warps.restype = I
         L.kvq_refresh_lens.argtypes = [P, P]
         L.kvq_last_error.argtypes = [P]
         L.kvq_last_error.restype = ctypes.c_char_p
@@ -314,6 +316,10 @@ class KVQCache:
     def kvq_set_decode_kernel(self, which: int):
         """0: compile-time specialisation when one matches (default); 1: generic kernel."""
         _check(lib().kvq_set_decode_kernel(self.handle, int(which)), "kvq_set_decode_kernel", self.handle)
+
+    def kvq_decode_cta_warps(self, fused: bool = False) -> int:
+        """Warps per CTA of the current decode (fused: decode-step) kernel; 0 if the step runs two kernels."""
+        return int(lib().kvq_decode_cta_warps(self.handle, int(bool(fused))))
 
     def kvq_decode_kernel_specialized(self) -> bool:
         return bool(lib().kvq_decode_kernel_specialized(self.handle))

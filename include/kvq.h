@@ -295,6 +295,12 @@ kvq_status kvq_set_decode_kernel(kvq_cache_t cache, int which);
 /* 1 if kvq_decode_attn currently runs a compile-time specialisation, else 0. */
 int kvq_decode_kernel_specialized(kvq_cache_t cache);
 
+/* Warps per CTA of the kernel kvq_decode_attn (fused == 0) or
+ * kvq_append_decode_attn (fused != 0) currently launches: 4 or 1 (see bit 2 of
+ * kvq_set_decode_kernel); 0 for a null handle, or for fused != 0 when that call
+ * runs the append and decode kernels one after the other. */
+int kvq_decode_cta_warps(kvq_cache_t cache, int fused);
+
 /* Replayed graphs advance the device lengths only; this copies them back into
  * the host mirror (synchronises `stream`). */
 kvq_status kvq_refresh_lens(kvq_cache_t cache, void* stream);

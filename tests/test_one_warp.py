@@ -106,3 +106,19 @@ def test_one_warp_window_decode_and_steps():
     ov = oracle_tensor(v, lens, c.tcap, wl.v, False, window)
     assert rel_err_rows(out.cpu().numpy(), decode_ref(wl, ok, ov, lens, q, scale, window)).max() <= TOL
     assert run_steps(wl, [200, 63, 500], 36, fused_kernel_bits=ONE_WARP, window=window, check_every=12) == {1}
+
+
+def test_cta_warps_query():
+    """kvq_decode_cta_warps reports the shape each call launches: one warp only
+    where the format has that specialisation and bit 2 asks for it; 0 for the
+    decode step when it runs two kernels (the generic kernel has no fused form)."""
+    wl = W("shape", 2, 4, 4, 128, *FMT, seed=25)
+    c = make_cache(wl, max_tokens=64)
+    assert (c.kvq_decode_cta_warps(), c.kvq_decode_cta_warps(True)) == (4, 4)
+    c.kvq_set_decode_kernel(ONE_WARP)
+    assert (c.kvq_decode_cta_warps(), c.kvq_decode_cta_warps(True)) == (1, 1)
+    c.kvq_set_decode_kernel(ONE_WARP | 1)  # the generic kernel: four warps, no fused step
+    assert (c.kvq_decode_cta_warps(), c.kvq_decode_cta_warps(True)) == (4, 0)
+    other = make_cache(W("other", 2, 4, 4, 64, (4, 32, PC, ASYM), (4, 32, PT, ASYM), seed=25), max_tokens=64)
+    other.kvq_set_decode_kernel(ONE_WARP)  # no one-warp specialisation for this format
+    assert (other.kvq_decode_cta_warps(), other.kvq_decode_cta_warps(True)) == (4, 4)
