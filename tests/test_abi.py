@@ -83,6 +83,15 @@ def test_capacity_and_buffer_checks(L):
     assert L.kvq_append_decode_attn(None, 0, None, None, 0, None, 0, 0.0, None, None) == 1
 
 
+def test_decode_kernel_choice_without_a_handle(L):
+    """The decode-kernel switches and queries refuse a null handle before any CUDA call."""
+    for which in (0, 4, 7, 8, -1):
+        assert L.kvq_set_decode_kernel(None, which) == 1
+    assert L.kvq_decode_cta_warps(None, 0) == 0
+    assert L.kvq_decode_cta_warps(None, 1) == 0
+    assert L.kvq_decode_kernel_specialized(None) == 0
+
+
 @pytest.mark.parametrize("window", [0, 64])
 @pytest.mark.parametrize("k,v,meta_f32", [
     ((4, 32, 1, 0), (4, 32, 0, 0), 0), ((2, 64, 1, 0), (2, 64, 0, 0), 0), ((6, 64, 0, 0), (4, 64, 0, 0), 0),
