@@ -76,21 +76,31 @@ def _check(name, out, k, v, q, wl, lens, tcap, scale):
     print(f"\n{name}: row {worst[0]:.2e} elementwise {worst[1]:.2e}")
 
 
-def _build(name, window=0):
+def _build(name, window=0, kernel_bits=0):
     wl = synth.workload(name, layers=1)
     cap = wl.max_tokens + 8
     cfg = kvq.make_config(1, wl.batch, wl.q_heads, wl.kv_heads, wl.head_dim, cap, wl.k, wl.v,
                           recent_window=window)
     cache = kvq.KVQCache(cfg)
+    if kernel_bits:
+        cache.kvq_set_decode_kernel(kernel_bits)
     cache.kvq_set_decode_plan(cap)
     k, v = wl.layer_kv(0, "cuda", T=wl.max_tokens)
     cache.kvq_prefill_quantize(0, k, v, wl.lens)
     return wl, cache, k, v
 
 
-@pytest.mark.parametrize("name", NAMES)
+# the workloads bench.py may time in one-warp CTAs (kvq_set_decode_kernel bit 2):
+# the formats that have one-warp kernels
+ONE_WARP = ["llama2_13b_kc_vt"]
+
+
+@pytest.mark.parametrize("name", NAMES + [n + "@one_warp" for n in ONE_WARP])
 def test_full_size_sampled_parity(name):
-    wl, cache, k, v = _build(name)
+    base, _, shape = name.partition("@")
+    wl, cache, k, v = _build(base, kernel_bits=4 if shape else 0)
+    if shape:
+        assert cache.kvq_decode_cta_warps() == 1
     q = wl.layer_query(0, 0, "cuda")
     scale = np.float32(1.0 / np.sqrt(wl.head_dim))
     out = cache.kvq_decode_attn(0, q, scale=float(scale))
@@ -99,14 +109,18 @@ def test_full_size_sampled_parity(name):
     _check(name, out.cpu().numpy(), k, v, q, wl, wl.lens, cache.tcap, scale)
 
 
-@pytest.mark.parametrize("name", NAMES)
+@pytest.mark.parametrize("name", NAMES + [n + "@one_warp" for n in ONE_WARP])
 def test_full_size_fused_step_sampled_parity(name):
     """One decode step of the benchmark's step graph at full size: the new
     token's append (fused into the decode launch when the format has a fused
     specialisation, else the append and decode kernels back to back), planned
-    for the capacity.  Sampled (sequence, kv head) outputs against the
-    oracle's quantization of the prefix plus the new token."""
-    wl, cache, k, v = _build(name)
+    for the capacity, in four-warp CTAs and, for the formats that have them,
+    one-warp CTAs.  Sampled (sequence, kv head) outputs against the oracle's
+    quantization of the prefix plus the new token."""
+    base, _, shape = name.partition("@")
+    wl, cache, k, v = _build(base, kernel_bits=4 if shape else 0)
+    if shape:
+        assert cache.kvq_decode_cta_warps(True) == 1
     kn, vn = wl.step_kv(0, 0, "cuda")
     q = wl.layer_query(0, 1, "cuda")
     scale = np.float32(1.0 / np.sqrt(wl.head_dim))
@@ -129,12 +143,13 @@ def test_full_size_fused_step_sampled_parity(name):
     _check(name, out.cpu().numpy(), kx, vx, q, wl, lens, cache.tcap, scale)
 
 
-@pytest.mark.parametrize("name", ["llama2_13b_kc_vt", "serving_mix", "wide_gqa_k4v8_kt"])
+@pytest.mark.parametrize("name", ["llama2_13b_kc_vt", "serving_mix", "wide_gqa_k4v8_kt", "llama2_13b_kc_vt@one_warp"])
 def test_full_size_window_sampled_parity(name):
     """bench.py --window 128: the newest 128 tokens of both tensors stay fp16
     rows; the oracle quantizes the older tokens with the same window."""
     window = 128
-    wl, cache, k, v = _build(name, window)
+    base, _, shape = name.partition("@")
+    wl, cache, k, v = _build(base, window, kernel_bits=4 if shape else 0)
     q = wl.layer_query(0, 0, "cuda")
     scale = np.float32(1.0 / np.sqrt(wl.head_dim))
     out = cache.kvq_decode_attn(0, q, scale=float(scale))
